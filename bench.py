@@ -1,0 +1,461 @@
+#!/usr/bin/env python
+"""Benchmark of the fused conv2d + BatchNorm + SiLU layer on GB300.
+
+One *step* is one pass of the whole hot path -- BN fold, then the fused
+forward -- over each of the five YOLO-shaped layers (tiny, stem, downsample,
+pointwise, deep), each on its own synthetic input.  ``value`` is the step's
+algorithmic work (2*M*C_out*C*R*S summed over the layers, padding not
+counted) divided by the device time of the timed steps, in TFLOP/s, summed
+over ranks (each rank runs its own replica: weak scaling, no collective on
+the data path).
+
+Timing: W warm-up steps, then K steps between two CUDA events on the
+launching stream, bracketed by a barrier and torch.cuda.synchronize() on
+both sides; max over ranks.  Inputs rotate over 3 buffer sets (about 426 MB
+touched per rotation, more than three times the 129 MB L2), so each step
+reads its data from HBM.  Per-kernel launch times come from CUDA events
+recorded around the forward calls inside the same timed region.  SM clocks
+and throttle reasons are sampled with nvidia-smi during the timed region.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead
+(the reference arm; a bounded sample of the same workload per step).
+
+Prints exactly one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from conv2d_batchnorm_silu_gb300.synthetic import (LAYERS, LAYER_ORDER,  # noqa: E402
+                                                   bits_to_torch_bf16, make_layer_inputs)
+
+METRIC = "fused conv+BN+SiLU TFLOP/s and % of conv roofline on 1 GB300"
+UNIT = "TFLOP/s"
+WORKLOAD = ("five YOLO-shaped fused conv+BN+SiLU layers per step, each BN fold + fused forward once: "
+            "tiny 1x32x32x16->32 3x3s1p1, stem 1x640x640x3->16 3x3s2p1, "
+            "down 16x160x160x64->128 3x3s2p1, pointwise 16x40x40x256->256 1x1, "
+            "deep 32x20x20x512->512 3x3s1p1; NHWC bf16 x, KRSC bf16 W, fp32 BN")
+DOMINANT = "deep"
+ROTATION = 3
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CLOCK_FIELDS = ("uuid,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--reference-budget-seconds", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world: int, use_cuda: bool):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend="nccl" if use_cuda else "gloo",
+                                             init_method="env://")
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest `value` across ranks (every rank receives it)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+# ------------------------------------------------------------------ peaks, clocks
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+
+    def __init__(self, uuid: str | None, interval_ms: int = 100):
+        self.uuid = uuid
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        return summarize_clocks(out, self.uuid)
+
+
+def summarize_clocks(csv_text: str, uuid: str | None) -> dict | None:
+    sm, sm_max, power, reasons = [], [], [], set()
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    for line in csv_text.splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        if uuid and uuid not in parts[0]:
+            continue
+        try:
+            sm.append(float(parts[2]))
+            sm_max.append(float(parts[3]))
+            power.append(float(parts[4]))
+        except ValueError:
+            continue
+        for name, val in zip(names, parts[6:10]):
+            if val.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(sm_max),
+            "power_w_max": max(power) if power else None, "samples": len(sm),
+            "reasons": sorted(reasons)}
+
+
+def device_uuid(dev_index: int) -> str | None:
+    try:
+        u = torch.cuda.get_device_properties(dev_index).uuid
+        return str(u)
+    except Exception:
+        return None
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "conv2d_batchnorm_silu_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(layer: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    ent = d.get("layers", {}).get(layer)
+    return float(ent["dram_bytes_per_launch"]) if ent else None
+
+
+# ------------------------------------------------------------------ the GPU arm
+class LayerBuffers:
+    """Device tensors of one layer instance (inputs, folded BN, output)."""
+
+    def __init__(self, inp, dev):
+        sh = inp.shape
+        self.shape = sh
+        self.x = bits_to_torch_bf16(inp.x_bits).to(dev)
+        self.w = bits_to_torch_bf16(inp.w_bits).to(dev)
+        self.g, self.b, self.m, self.v = (torch.from_numpy(a).to(dev)
+                                          for a in (inp.gamma, inp.beta, inp.mean, inp.var))
+        self.eps = inp.eps
+        self.scale = torch.empty(sh.k, dtype=torch.float32, device=dev)
+        self.bias = torch.empty(sh.k, dtype=torch.float32, device=dev)
+        self.y = torch.empty((sh.n, sh.ho, sh.wo, sh.k), dtype=torch.bfloat16, device=dev)
+
+
+def run_ours(args, rank, world, local_rank):
+    from conv2d_batchnorm_silu_gb300 import _build
+    _build.build()
+    from conv2d_batchnorm_silu_gb300 import capi
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist_init(world, True)
+    stream = torch.cuda.current_stream(dev)
+    inputs = {name: make_layer_inputs(LAYERS[name]) for name in LAYER_ORDER}
+    sets = [{name: LayerBuffers(inputs[name], dev) for name in LAYER_ORDER} for _ in range(ROTATION)]
+    flops_step = sum(LAYERS[n].flops for n in LAYER_ORDER)
+    launches_per_step = 2 * len(LAYER_ORDER)
+
+    def step(i, ev=None):
+        bufs = sets[i % ROTATION]
+        for name in LAYER_ORDER:
+            lb = bufs[name]
+            sh = lb.shape
+            capi.fold(lb.g, lb.b, lb.m, lb.v, lb.eps, lb.scale, lb.bias, stream=stream)
+            if ev is not None:
+                ev[name][0].record(stream)
+            capi.forward(lb.x, lb.w, lb.scale, lb.bias, sh.stride, sh.pad, y=lb.y, stream=stream)
+            if ev is not None:
+                ev[name][1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    capi.check(stream)
+
+    K = args.steps
+    per_kernel = {name: ([torch.cuda.Event(enable_timing=True) for _ in range(K)],
+                         [torch.cuda.Event(enable_timing=True) for _ in range(K)])
+                  for name in LAYER_ORDER}
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device_uuid(local_rank))
+    time.sleep(0.3)  # let the sampler start
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        step(i, {n: (per_kernel[n][0][i], per_kernel[n][1][i]) for n in LAYER_ORDER})
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    capi.check(stream)
+    elapsed_s = start.elapsed_time(end) / 1e3
+    elapsed_max = max_over_ranks(elapsed_s, world, dev)
+    per_layer_us = {n: 1e3 * float(np.mean([a.elapsed_time(b) for a, b in zip(*per_kernel[n])]))
+                    for n in LAYER_ORDER}
+
+    peaks, peak_src = load_peaks()
+    per_layer = {}
+    for n in LAYER_ORDER:
+        sh = LAYERS[n]
+        t = per_layer_us[n] * 1e-6
+        roof = max(sh.flops / (peaks["bf16_tflops"] * 1e12), sh.compulsory_bytes / (peaks["hbm_gbs"] * 1e9))
+        plan = capi.plan(sh.n, sh.h, sh.w, sh.c, sh.k, sh.r, sh.s, sh.stride, sh.pad)
+        per_layer[n] = {"us_per_call": round(per_layer_us[n], 3),
+                        "tflops": round(sh.flops / t / 1e12, 2),
+                        "gbs": round(sh.compulsory_bytes / t / 1e9, 1),
+                        "roofline_us": round(roof * 1e6, 3),
+                        "roofline_frac": round(roof / t, 4),
+                        "bound": "tensor" if sh.flops / (peaks["bf16_tflops"] * 1e12) >=
+                                 sh.compulsory_bytes / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                        "kernel": plan["algo"], "tile": [plan["block_m"], plan["block_n"], plan["block_k"]],
+                        "grid": plan["grid"]}
+    dom = LAYERS[DOMINANT]
+    dom_t = per_layer_us[DOMINANT] * 1e-6
+    achieved = dom.flops / dom_t / 1e12
+    traffic = recorded_traffic(DOMINANT)
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": traffic, "kernel": f"{DOMINANT} layer forward ({per_layer[DOMINANT]['kernel']})",
+                "peak_source": f"{peak_src} bf16 dense (burst)",
+                "algorithmic_flops_per_launch": dom.flops}
+
+    e2e = run_e2e(args, capi, inputs, dev, stream, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_baseline_seconds)
+
+    value = aggregate_throughput(flops_step * K, world, elapsed_max) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_max / K * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded PCG64: x~N(0,1), W~N(0,2/fan_in), BN gamma~U(.5,1.5), "
+                "beta,mean~N(0,.1), var~U(.5,2), eps=1e-3)",
+        "config": {"workload": WORKLOAD, "flops_per_step": flops_step,
+                   "l2": f"{ROTATION} rotating buffer sets (~426 MB per rotation > 129 MB L2)",
+                   "parallelism": f"replicas x{world} (each rank runs the full step)"},
+        "roofline": roofline,
+        "per_layer": per_layer,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "peaks": {**peaks, "source": peak_src},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+def run_e2e(args, capi, inputs, dev, stream, world):
+    """Same metric through the public API with host buffers: per step, every layer's x goes
+    host->device from pinned memory, the fold and fused forward run, and y comes back
+    device->host into pinned memory.  Weights and BN statistics stay resident on the device."""
+    host_x = {n: bits_to_torch_bf16(inputs[n].x_bits).pin_memory() for n in LAYER_ORDER}
+    bufs = {n: LayerBuffers(inputs[n], dev) for n in LAYER_ORDER}
+    host_y = {n: torch.empty(bufs[n].y.shape, dtype=torch.bfloat16).pin_memory() for n in LAYER_ORDER}
+    h2d = sum(t.numel() * 2 for t in host_x.values())
+    d2h = sum(t.numel() * 2 for t in host_y.values())
+    flops_step = sum(LAYERS[n].flops for n in LAYER_ORDER)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for n in LAYER_ORDER:
+                b = bufs[n]
+                sh = b.shape
+                b.x.copy_(host_x[n], non_blocking=True)
+                capi.fold(b.g, b.b, b.m, b.v, b.eps, b.scale, b.bias, stream=stream)
+                capi.forward(b.x, b.w, b.scale, b.bias, sh.stride, sh.pad, y=b.y, stream=stream)
+                host_y[n].copy_(b.y, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t = max_over_ranks(s.elapsed_time(e) / 1e3, world, dev)
+    return {"value": round(aggregate_throughput(flops_step * args.e2e_steps, world, t) / 1e12, 3),
+            "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(t / args.e2e_steps * 1e3, 4), "steps": args.e2e_steps,
+            "api": "conv2d_batchnorm_silu_gb300.capi.fold/forward on the C ABI, pinned host buffers"}
+
+
+# ------------------------------------------------------------------ the oracle (CPU) legs
+def oracle_sample_step(pixels_per_layer: dict, inputs) -> int:
+    """One oracle pass over a sample of output pixels of every layer; returns its flops."""
+    import oracle
+    flops = 0
+    for n in LAYER_ORDER:
+        inp = inputs[n]
+        sh = inp.shape
+        pix = pixels_per_layer[n]
+        oracle.conv_bn_silu_at(inp.x_bits, inp.w_bits, inp.gamma, inp.beta, inp.mean, inp.var,
+                               inp.eps, pix, sh.stride, sh.pad)
+        flops += 2 * pix.size * sh.k * sh.kdim
+    return flops
+
+
+def sample_pixels(fraction: float, inputs, seed: int = 0) -> dict:
+    """The same fraction of every layer's output pixels (at least one), chosen evenly."""
+    out = {}
+    for n in LAYER_ORDER:
+        m = inputs[n].shape.m
+        cnt = max(1, int(round(m * fraction)))
+        out[n] = np.linspace(0, m - 1, cnt).astype(np.int64)
+    return out
+
+
+def cpu_baseline(seconds: float) -> dict:
+    """The oracle as it stands, on this host's cores, over a bounded sample of the workload."""
+    import oracle
+    inputs = {n: make_layer_inputs(LAYERS[n]) for n in LAYER_ORDER}
+    frac = 1e-4
+    t0 = time.perf_counter()
+    flops = oracle_sample_step(sample_pixels(frac, inputs), inputs)
+    dt = time.perf_counter() - t0
+    # scale the sample so the timed pass takes about `seconds`
+    frac = min(1.0, frac * max(1.0, seconds / max(dt, 1e-3)))
+    pix = sample_pixels(frac, inputs)
+    t0 = time.perf_counter()
+    flops = oracle_sample_step(pix, inputs)
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": oracle.default_threads(),
+            "kind": "oracle",
+            "sample": f"{frac:.3g} of every layer's output pixels (evenly spaced, all channels), "
+                      f"{sum(p.size for p in pix.values())} pixels, {flops / 1e9:.2f} GFLOP in {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle, timed on the host cores, per step a sample."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inputs = {n: make_layer_inputs(LAYERS[n]) for n in LAYER_ORDER}
+    total_steps = max(1, args.steps + args.warmup)
+    target_step_s = max(1e-3, args.reference_budget_seconds / total_steps)
+    frac = 1e-5
+    t0 = time.perf_counter()
+    oracle_sample_step(sample_pixels(frac, inputs), inputs)
+    dt = time.perf_counter() - t0
+    frac = min(1.0, frac * max(1.0, target_step_s / max(dt, 1e-4)))
+    pix = sample_pixels(frac, inputs)
+    for _ in range(args.warmup):
+        oracle_sample_step(pix, inputs)
+    t0 = time.perf_counter()
+    flops = 0
+    for _ in range(args.steps):
+        flops += oracle_sample_step(pix, inputs)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"per step {frac:.3g} of every layer's output pixels "
+              f"({sum(p.size for p in pix.values())} pixels, all channels)")
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded inputs as the GPU arm)",
+        "config": {"workload": WORKLOAD, "l2": "n/a (CPU)", "parallelism": "host threads"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": oracle.default_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local_rank)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+"""Python binding of the C ABI in ``include/conv_bn_silu.h`` (ctypes).
+
+Argument marshalling only: every step of the layer runs in the CUDA library
+``libconvbnsilu.so``; this module checks tensor dtypes/layouts, passes raw
+device pointers, sizes and the current CUDA stream, and turns status codes
+into exceptions.  PyTorch supplies device memory and streams.  There is no
+fallback: if the library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libconvbnsilu.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()' "
+        "or conv2d_batchnorm_silu_gb300._build.build()); there is no non-CUDA fallback")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+CBS_OK = 0
+CBS_ERR_INVALID_ARG = 1
+CBS_ERR_MISALIGNED = 2
+CBS_ERR_UNSUPPORTED = 3
+CBS_ERR_CUDA = 4
+CBS_ERR_TIMEOUT = 5
+
+ALGOS = {"auto": 0, "tcgen05": 1, "direct": 2}
+ALGO_NAMES = {v: k for k, v in ALGOS.items()}
+
+_i = ctypes.c_int
+_p = ctypes.c_void_p
+_f = ctypes.c_float
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int) for name in (
+        "algo", "block_m", "block_n", "block_k", "stages", "tiles", "grid", "threads",
+        "smem_bytes", "k_iters")]
+
+    def as_dict(self) -> dict:
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["algo"] = ALGO_NAMES.get(d["algo"], d["algo"])
+        return d
+
+
+def _declare(name, argtypes, restype=ctypes.c_int):
+    fn = getattr(_lib, name)
+    fn.argtypes = argtypes
+    fn.restype = restype
+    return fn
+
+
+_fold = _declare("conv_bn_silu_fold", [_p, _p, _p, _p, _f, _i, _p, _p, _p])
+_forward = _declare("conv_bn_silu_forward", [_p] * 5 + [_i] * 11 + [_p])
+_forward_algo = _declare("conv_bn_silu_forward_algo", [_p] * 5 + [_i] * 12 + [_p])
+_output_dims = _declare("conv_bn_silu_output_dims", [_i] * 8 + [ctypes.POINTER(_i)] * 2)
+_plan = _declare("conv_bn_silu_plan", [_i] * 13 + [ctypes.POINTER(PlanInfo)])
+_check = _declare("conv_bn_silu_check", [_p])
+_status_string = _declare("conv_bn_silu_status_string", [_i], ctypes.c_char_p)
+_last_cuda_error = _declare("conv_bn_silu_last_cuda_error", [])
+
+
+class CbsError(RuntimeError):
+    """A non-zero cbs_status from the C library."""
+
+    def __init__(self, status: int, what: str):
+        msg = _status_string(status).decode()
+        if status == CBS_ERR_CUDA:
+            msg += f" (cudaError {_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}")
+        self.status = status
+
+
+def _raise_if(status: int, what: str) -> None:
+    if status != CBS_OK:
+        raise CbsError(status, what)
+
+
+def _pair(v) -> tuple[int, int]:
+    if isinstance(v, (tuple, list)):
+        return int(v[0]), int(v[1])
+    return int(v), int(v)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev_tensor(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (NHWC / KRSC dense)")
+    return t.data_ptr()
+
+
+def output_dims(h: int, w: int, r: int, s: int, stride=1, pad=0) -> tuple[int, int]:
+    """(ho, wo) of the convolution; host only."""
+    sh, sw = _pair(stride)
+    ph, pw = _pair(pad)
+    ho, wo = _i(), _i()
+    _raise_if(_output_dims(h, w, r, s, sh, sw, ph, pw, ctypes.byref(ho), ctypes.byref(wo)),
+              "conv_bn_silu_output_dims")
+    return ho.value, wo.value
+
+
+def plan(n, h, w, c, c_out, r, s, stride=1, pad=0, algo="auto", sm_count: int = 152) -> dict:
+    """The tile plan conv_bn_silu_forward_algo would use; host only."""
+    sh, sw = _pair(stride)
+    ph, pw = _pair(pad)
+    info = PlanInfo()
+    _raise_if(_plan(n, h, w, c, c_out, r, s, sh, sw, ph, pw, ALGOS[algo], sm_count,
+                    ctypes.byref(info)), "conv_bn_silu_plan")
+    return info.as_dict()
+
+
+def fold(gamma: torch.Tensor, beta: torch.Tensor, mean: torch.Tensor, var: torch.Tensor,
+         eps: float, scale: torch.Tensor | None = None, bias: torch.Tensor | None = None,
+         stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """conv_bn_silu_fold: per-channel fp32 scale and bias from BN statistics (device)."""
+    c_out = gamma.numel()
+    for t, nm in ((beta, "beta"), (mean, "mean"), (var, "var")):
+        if t.numel() != c_out:
+            raise ValueError(f"{nm} has {t.numel()} elements, expected {c_out}")
+    if scale is None:
+        scale = torch.empty(c_out, dtype=torch.float32, device=gamma.device)
+    if bias is None:
+        bias = torch.empty(c_out, dtype=torch.float32, device=gamma.device)
+    ptrs = [_dev_tensor(t, torch.float32, nm) for t, nm in
+            ((gamma, "gamma"), (beta, "beta"), (mean, "mean"), (var, "var"),
+             (scale, "scale"), (bias, "bias"))]
+    _raise_if(_fold(ptrs[0], ptrs[1], ptrs[2], ptrs[3], float(eps), c_out, ptrs[4], ptrs[5],
+                    _stream_handle(stream)), "conv_bn_silu_fold")
+    return scale, bias
+
+
+def forward(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor, bias: torch.Tensor,
+            stride=1, pad=0, y: torch.Tensor | None = None, algo: str = "auto",
+            stream=None) -> torch.Tensor:
+    """conv_bn_silu_forward(_algo): y = SiLU(conv2d(x, w) * scale + bias).
+
+    x: bf16 NHWC [n, h, w, c]; w: bf16 KRSC [c_out, r, s, c]; scale/bias: fp32 [c_out];
+    y (optional, allocated if None): bf16 NHWC [n, ho, wo, c_out].
+    """
+    if x.dim() != 4 or w.dim() != 4:
+        raise ValueError("x must be NHWC and w KRSC (4-D)")
+    n, h, wi, c = x.shape
+    c_out, r, s, c2 = w.shape
+    if c2 != c:
+        raise ValueError(f"channel mismatch: x has {c}, w has {c2}")
+    if scale.numel() != c_out or bias.numel() != c_out:
+        raise ValueError("scale and bias must have c_out elements")
+    sh, sw = _pair(stride)
+    ph, pw = _pair(pad)
+    ho, wo = output_dims(h, wi, r, s, (sh, sw), (ph, pw))
+    if y is None:
+        y = torch.empty((n, ho, wo, c_out), dtype=torch.bfloat16, device=x.device)
+    elif tuple(y.shape) != (n, ho, wo, c_out):
+        raise ValueError(f"y has shape {tuple(y.shape)}, expected {(n, ho, wo, c_out)}")
+    if y.numel() == 0:
+        return y
+    px = _dev_tensor(x, torch.bfloat16, "x")
+    pw_ = _dev_tensor(w, torch.bfloat16, "w")
+    ps = _dev_tensor(scale, torch.float32, "scale")
+    pb = _dev_tensor(bias, torch.float32, "bias")
+    py = _dev_tensor(y, torch.bfloat16, "y")
+    st = _forward_algo(px, pw_, ps, pb, py, n, h, wi, c, c_out, r, s, sh, sw, ph, pw,
+                       ALGOS[algo], _stream_handle(stream))
+    _raise_if(st, "conv_bn_silu_forward")
+    return y
+
+
+def forward_ptr(x_ptr: int, w_ptr: int, scale_ptr: int, bias_ptr: int, y_ptr: int,
+                n, h, w, c, c_out, r, s, stride=1, pad=0, algo: str = "auto",
+                stream=None) -> None:
+    """conv_bn_silu_forward_algo on raw device pointers (for callers that manage memory)."""
+    sh, sw = _pair(stride)
+    ph, pw = _pair(pad)
+    _raise_if(_forward_algo(x_ptr, w_ptr, scale_ptr, bias_ptr, y_ptr, n, h, w, c, c_out, r, s,
+                            sh, sw, ph, pw, ALGOS[algo], _stream_handle(stream)),
+              "conv_bn_silu_forward")
+
+
+def check(stream=None) -> None:
+    """conv_bn_silu_check: synchronise and raise if a kernel's pipeline wait timed out."""
+    _raise_if(_check(_stream_handle(stream)), "conv_bn_silu_check")
+
+
+def raw_status(fn_name: str, *args) -> int:
+    """Call one C entry point with raw arguments and return its status (for tests)."""
+    return getattr(_lib, fn_name)(*args)

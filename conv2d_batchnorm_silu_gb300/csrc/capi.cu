@@ -1,0 +1,225 @@
+// capi.cu -- the extern "C" boundary declared in include/conv_bn_silu.h:
+// argument validation, output sizes, kernel choice and launch, error words.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/conv_bn_silu.h"
+#include "cbs_internal.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = (int)e;
+    return CBS_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int dims_from(int h, int w_in, int r, int s, int sh, int sw, int ph, int pw, int *ho, int *wo)
+{
+    if (h < 1 || w_in < 1 || r < 1 || s < 1 || sh < 1 || sw < 1 || ph < 0 || pw < 0)
+        return CBS_ERR_INVALID_ARG;
+    const long long hp = (long long)h + 2LL * ph, wp = (long long)w_in + 2LL * pw;
+    if (hp < r || wp < s) return CBS_ERR_INVALID_ARG;
+    const long long oh = (hp - r) / sh + 1, ow = (wp - s) / sw + 1;
+    if (oh < 1 || ow < 1 || oh > 0x7fffffffLL || ow > 0x7fffffffLL) return CBS_ERR_INVALID_ARG;
+    *ho = (int)oh;
+    *wo = (int)ow;
+    return CBS_OK;
+}
+
+// Shape checks shared by forward and plan.  Fills everything but the pointers.
+int make_problem(int n, int h, int w_in, int c, int c_out, int r, int s, int sh, int sw, int ph, int pw,
+                 cbs::ConvProblem *p)
+{
+    if (n < 0 || c < 1 || c_out < 0) return CBS_ERR_INVALID_ARG;
+    int ho = 0, wo = 0;
+    const int st = dims_from(h, w_in, r, s, sh, sw, ph, pw, &ho, &wo);
+    if (st != CBS_OK) return st;
+    p->n = n;
+    p->h = h;
+    p->w_in = w_in;
+    p->c = c;
+    p->c_out = c_out;
+    p->r = r;
+    p->s = s;
+    p->stride_h = sh;
+    p->stride_w = sw;
+    p->pad_h = ph;
+    p->pad_w = pw;
+    p->ho = ho;
+    p->wo = wo;
+    p->m = (long long)n * ho * wo;
+    // Keep every tensor's element count within 2^62 so byte offsets never overflow.
+    const long long xe = (long long)n * h * w_in;
+    if (xe > (1LL << 40) / (c > 0 ? c : 1) || p->m > (1LL << 40) / (c_out > 0 ? c_out : 1) ||
+        (long long)r * s * c > (1LL << 31) - 1)
+        return CBS_ERR_INVALID_ARG;
+    return CBS_OK;
+}
+
+int select_algo(const cbs::ConvProblem &p, int algo)
+{
+    if (algo == CBS_ALGO_AUTO) return cbs::tc_supported(p) ? CBS_ALGO_TCGEN05 : CBS_ALGO_DIRECT;
+    return algo;
+}
+
+int sm_count_current_device(int *count)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    static std::mutex mu;
+    static std::vector<int> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if ((int)cache.size() > dev && cache[dev] > 0) {
+            *count = cache[dev];
+            return CBS_OK;
+        }
+    }
+    int v = 0;
+    e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
+    cache[dev] = v;
+    *count = v;
+    return CBS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int conv_bn_silu_fold(const float *gamma, const float *beta, const float *mean, const float *var,
+                      float eps, int c_out, float *scale, float *bias, void *stream)
+{
+    if (c_out < 0 || !(eps >= 0.0f) || eps > 3.0e38f) return CBS_ERR_INVALID_ARG;
+    if (c_out == 0) return CBS_OK;
+    if (!gamma || !beta || !mean || !var || !scale || !bias) return CBS_ERR_INVALID_ARG;
+    if (!aligned16(gamma) || !aligned16(beta) || !aligned16(mean) || !aligned16(var) ||
+        !aligned16(scale) || !aligned16(bias))
+        return CBS_ERR_MISALIGNED;
+    cudaError_t e = cbs::fold_launch(gamma, beta, mean, var, eps, c_out, scale, bias,
+                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+}
+
+int conv_bn_silu_forward_algo(const void *x, const void *w, const float *scale, const float *bias,
+                              void *y, int n, int h, int w_in, int c, int c_out, int r, int s,
+                              int stride_h, int stride_w, int pad_h, int pad_w, int algo, void *stream)
+{
+    if (algo < CBS_ALGO_AUTO || algo > CBS_ALGO_DIRECT) return CBS_ERR_INVALID_ARG;
+    cbs::ConvProblem p{};
+    int st = make_problem(n, h, w_in, c, c_out, r, s, stride_h, stride_w, pad_h, pad_w, &p);
+    if (st != CBS_OK) return st;
+    if (p.m == 0 || c_out == 0) return CBS_OK;
+    if (!x || !w || !scale || !bias || !y) return CBS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(scale) || !aligned16(bias) || !aligned16(y))
+        return CBS_ERR_MISALIGNED;
+    p.x = x;
+    p.w = w;
+    p.scale = scale;
+    p.bias = bias;
+    p.y = y;
+    const int chosen = select_algo(p, algo);
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    if (chosen == CBS_ALGO_TCGEN05) {
+        if (!cbs::tc_supported(p)) return CBS_ERR_UNSUPPORTED;
+        int sms = 0;
+        st = sm_count_current_device(&sms);
+        if (st != CBS_OK) return st;
+        const cbs::TcPlan plan = cbs::tc_make_plan(p, sms);
+        cudaError_t e = cbs::tc_launch(p, plan, strm);
+        return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+    }
+    cudaError_t e = cbs::direct_launch(p, strm);
+    return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+}
+
+int conv_bn_silu_forward(const void *x, const void *w, const float *scale, const float *bias, void *y,
+                         int n, int h, int w_in, int c, int c_out, int r, int s, int stride_h,
+                         int stride_w, int pad_h, int pad_w, void *stream)
+{
+    return conv_bn_silu_forward_algo(x, w, scale, bias, y, n, h, w_in, c, c_out, r, s, stride_h,
+                                     stride_w, pad_h, pad_w, CBS_ALGO_AUTO, stream);
+}
+
+int conv_bn_silu_output_dims(int h, int w_in, int r, int s, int stride_h, int stride_w, int pad_h,
+                             int pad_w, int *ho, int *wo)
+{
+    if (!ho || !wo) return CBS_ERR_INVALID_ARG;
+    return dims_from(h, w_in, r, s, stride_h, stride_w, pad_h, pad_w, ho, wo);
+}
+
+int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, int stride_h, int stride_w,
+                      int pad_h, int pad_w, int algo, int sm_count, cbs_plan_info *info)
+{
+    if (!info || sm_count < 1 || algo < CBS_ALGO_AUTO || algo > CBS_ALGO_DIRECT)
+        return CBS_ERR_INVALID_ARG;
+    cbs::ConvProblem p{};
+    const int st = make_problem(n, h, w_in, c, c_out, r, s, stride_h, stride_w, pad_h, pad_w, &p);
+    if (st != CBS_OK) return st;
+    const int chosen = select_algo(p, algo);
+    cbs_plan_info out{};
+    out.algo = chosen;
+    if (chosen == CBS_ALGO_TCGEN05) {
+        if (!cbs::tc_supported(p)) return CBS_ERR_UNSUPPORTED;
+        const cbs::TcPlan t = cbs::tc_make_plan(p, sm_count);
+        out.block_m = cbs::kTcBlockM;
+        out.block_n = t.block_n;
+        out.block_k = t.block_k;
+        out.stages = t.stages;
+        out.tiles = t.tiles;
+        out.grid = t.grid;
+        out.threads = cbs::kTcThreads;
+        out.smem_bytes = t.smem_bytes;
+        out.k_iters = t.k_iters;
+    } else {
+        const long long bx = (p.m + cbs::kDirectThreads - 1) / cbs::kDirectThreads;
+        const int by = (c_out + cbs::kDirectBlockN - 1) / cbs::kDirectBlockN;
+        out.block_m = cbs::kDirectThreads;
+        out.block_n = cbs::kDirectBlockN;
+        out.block_k = 1;
+        out.stages = 0;
+        out.tiles = (int)(bx * by);
+        out.grid = out.tiles;
+        out.threads = cbs::kDirectThreads;
+        out.smem_bytes = 0;
+        out.k_iters = r * s * c;
+    }
+    *info = out;
+    return CBS_OK;
+}
+
+int conv_bn_silu_check(void *stream)
+{
+    unsigned int word = 0;
+    cudaError_t e = cbs::tc_read_and_clear_error(static_cast<cudaStream_t>(stream), &word);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return word != 0 ? CBS_ERR_TIMEOUT : CBS_OK;
+}
+
+const char *conv_bn_silu_status_string(int status)
+{
+    switch (status) {
+    case CBS_OK: return "ok";
+    case CBS_ERR_INVALID_ARG: return "invalid argument";
+    case CBS_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case CBS_ERR_UNSUPPORTED: return "shape not supported by the requested kernel";
+    case CBS_ERR_CUDA: return "CUDA error";
+    case CBS_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int conv_bn_silu_last_cuda_error(void) { return t_last_cuda_error; }
+
+}  // extern "C"

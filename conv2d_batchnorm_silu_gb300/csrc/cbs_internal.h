@@ -1,0 +1,60 @@
+// cbs_internal.h -- host-side types shared by the C ABI (capi.cu) and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cbs {
+
+// One convolution call, with the derived GEMM view M = n*ho*wo, N = c_out, K = c*r*s.
+struct ConvProblem {
+    const void *x;
+    const void *w;
+    const float *scale;
+    const float *bias;
+    void *y;
+    int n, h, w_in, c, c_out, r, s;
+    int stride_h, stride_w, pad_h, pad_w;
+    int ho, wo;
+    long long m;  // output pixels
+};
+
+// Tile configuration of the tcgen05 implicit GEMM.
+struct TcPlan {
+    int block_n;   // 16, 32, 64, 128 or 256 (UMMA N)
+    int block_k;   // 16, 32 or 64 channels per stage (= swizzle width / 2 bytes)
+    int stages;
+    int c_chunks;  // ceil(c / block_k)
+    int k_iters;   // r * s * c_chunks
+    int m_tiles, n_tiles, tiles;
+    int grid;
+    int smem_bytes;
+};
+
+constexpr int kTcBlockM = 128;
+constexpr int kTcThreads = 256;
+constexpr int kDirectThreads = 128;
+constexpr int kDirectBlockN = 16;
+
+// Planning (host only, no GPU needed).
+bool tc_supported(const ConvProblem &p);
+TcPlan tc_make_plan(const ConvProblem &p, int sm_count);
+int tc_smem_bytes(int block_n, int block_k, int stages);
+
+// Launchers; return cudaSuccess or the first CUDA error met.
+cudaError_t tc_launch(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream);
+cudaError_t direct_launch(const ConvProblem &p, cudaStream_t stream);
+cudaError_t fold_launch(const float *gamma, const float *beta, const float *mean, const float *var,
+                        float eps, int c_out, float *scale, float *bias, cudaStream_t stream);
+
+// Device error words (one per kernel translation unit): read and clear, stream-ordered.
+cudaError_t tc_read_and_clear_error(cudaStream_t stream, unsigned int *out);
+
+// Device error codes written by kernels (bit flags).
+constexpr unsigned int kErrTimeoutProducer = 1u;
+constexpr unsigned int kErrTimeoutMma = 2u;
+constexpr unsigned int kErrTimeoutEpilogue = 4u;
+constexpr unsigned int kErrTimeoutDrain = 8u;
+
+}  // namespace cbs

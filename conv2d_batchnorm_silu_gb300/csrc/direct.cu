@@ -1,0 +1,147 @@
+// direct.cu -- fused conv2d + BatchNorm + SiLU on the CUDA cores, any shape.
+//
+// The "scalar" member of the family in "Fusing an Epilogue" (kernels book,
+// section "Three kernels for one operation": one output element per lane, no
+// set-up cost): here one thread owns one output pixel and a group of 16
+// output channels, so the 16 accumulators stay in registers through the
+// whole (r, s, c) reduction and the epilogue (BN multiply/add, SiLU, bf16
+// cast) runs on them before the single store.  The block's 16 filters are
+// staged in shared memory as fp32, [tap][16], in chunks, and every thread
+// reads them as broadcast float4s.  It serves shapes the tensor-core kernel
+// does not take (c % 16 != 0, e.g. a 3-channel stem; c_out % 8 != 0).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "cbs_internal.h"
+#include "epilogue.cuh"
+
+namespace cbs {
+namespace {
+
+constexpr int KB = kDirectBlockN;     // output channels per thread
+constexpr int QCH = 512;              // filter taps (r, s, c) staged per chunk: 32 KB
+
+struct DirectArgs {
+    const __nv_bfloat16 *x;
+    const __nv_bfloat16 *w;
+    const float *scale;
+    const float *bias;
+    __nv_bfloat16 *y;
+    long long m;
+    int h, w_in, c, c_out, r, s;
+    int stride_h, stride_w, pad_h, pad_w, ho, wo;
+};
+
+__global__ void __launch_bounds__(kDirectThreads)
+    direct_conv_bn_silu_kernel(const DirectArgs a)
+{
+    __shared__ __align__(16) float wsm[QCH][KB];
+    const long long m = (long long)blockIdx.x * kDirectThreads + threadIdx.x;
+    const int k0 = blockIdx.y * KB;
+    const bool active = m < a.m;
+    int ow = 0, oh = 0, img = 0;
+    if (active) {
+        ow = (int)(m % a.wo);
+        const long long t = m / a.wo;
+        oh = (int)(t % a.ho);
+        img = (int)(t / a.ho);
+    }
+    float acc[KB];
+#pragma unroll
+    for (int j = 0; j < KB; ++j) acc[j] = 0.f;
+
+    const int taps = a.r * a.s * a.c;
+    for (int q0 = 0; q0 < taps; q0 += QCH) {
+        const int qn = min(QCH, taps - q0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < qn * KB; i += kDirectThreads) {
+            const int q = i / KB, j = i - q * KB;
+            const int k = k0 + j;
+            wsm[q][j] = k < a.c_out ? __bfloat162float(a.w[(long long)k * taps + q0 + q]) : 0.f;
+        }
+        __syncthreads();
+        if (active) {
+            int c = q0 % a.c;
+            int rs = q0 / a.c;
+            int s = rs % a.s;
+            int r = rs / a.s;
+            for (int q = 0; q < qn; ++q) {
+                const int ih = oh * a.stride_h - a.pad_h + r;
+                const int iw = ow * a.stride_w - a.pad_w + s;
+                if (ih >= 0 && ih < a.h && iw >= 0 && iw < a.w_in) {
+                    const float xv = __bfloat162float(
+                        a.x[(((long long)img * a.h + ih) * a.w_in + iw) * a.c + c]);
+                    const float4 *wq = reinterpret_cast<const float4 *>(wsm[q]);
+#pragma unroll
+                    for (int j4 = 0; j4 < KB / 4; ++j4) {
+                        const float4 wv = wq[j4];
+                        acc[4 * j4 + 0] = fmaf(xv, wv.x, acc[4 * j4 + 0]);
+                        acc[4 * j4 + 1] = fmaf(xv, wv.y, acc[4 * j4 + 1]);
+                        acc[4 * j4 + 2] = fmaf(xv, wv.z, acc[4 * j4 + 2]);
+                        acc[4 * j4 + 3] = fmaf(xv, wv.w, acc[4 * j4 + 3]);
+                    }
+                }
+                if (++c == a.c) {
+                    c = 0;
+                    if (++s == a.s) {
+                        s = 0;
+                        ++r;
+                    }
+                }
+            }
+        }
+    }
+    if (!active) return;
+    // Epilogue on the registers: BN multiply/add, SiLU, bf16, one store per channel pair.
+    __nv_bfloat16 *yp = a.y + m * a.c_out + k0;
+    if (k0 + KB <= a.c_out && (a.c_out % 8) == 0) {
+        uint32_t packed[KB / 2];
+#pragma unroll
+        for (int j = 0; j < KB; j += 2)
+            packed[j / 2] = dev::pack_bf16x2(dev::bn_silu(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j)),
+                                             dev::bn_silu(acc[j + 1], __ldg(a.scale + k0 + j + 1),
+                                                          __ldg(a.bias + k0 + j + 1)));
+        uint4 *dst = reinterpret_cast<uint4 *>(yp);
+#pragma unroll
+        for (int v = 0; v < KB / 8; ++v)
+            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+            if (k0 + j < a.c_out)
+                yp[j] = __float2bfloat16_rn(dev::bn_silu(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j)));
+    }
+}
+
+}  // namespace
+
+cudaError_t direct_launch(const ConvProblem &p, cudaStream_t stream)
+{
+    DirectArgs a;
+    a.x = static_cast<const __nv_bfloat16 *>(p.x);
+    a.w = static_cast<const __nv_bfloat16 *>(p.w);
+    a.scale = p.scale;
+    a.bias = p.bias;
+    a.y = static_cast<__nv_bfloat16 *>(p.y);
+    a.m = p.m;
+    a.h = p.h;
+    a.w_in = p.w_in;
+    a.c = p.c;
+    a.c_out = p.c_out;
+    a.r = p.r;
+    a.s = p.s;
+    a.stride_h = p.stride_h;
+    a.stride_w = p.stride_w;
+    a.pad_h = p.pad_h;
+    a.pad_w = p.pad_w;
+    a.ho = p.ho;
+    a.wo = p.wo;
+    const long long bx = (p.m + kDirectThreads - 1) / kDirectThreads;
+    if (bx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    dim3 grid((unsigned)bx, (unsigned)((p.c_out + KB - 1) / KB));
+    if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+    direct_conv_bn_silu_kernel<<<grid, kDirectThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace cbs

@@ -1,0 +1,640 @@
+// tc_conv.cu -- fused conv2d + BatchNorm + SiLU as an implicit GEMM on the
+// sm_103a tensor cores.
+//
+// GEMM view ("Fusing an Epilogue", kernels book, section "Three kernels for
+// one operation": convolution as a GEMM on the tensor cores):
+//   M = n*ho*wo output pixels, N = c_out, K = r*s*c, ordered (r, s, c) so that
+//   the KRSC weight tensor is already the K-major B operand.
+//   A[m][k] = x[img][oh*sh - ph + r][ow*sw - pw + s][c], zero outside the image.
+//
+// Per CTA (one per SM, persistent over output tiles of 128 pixels x BN channels):
+//   warp 0      TMA producer: per K step, one im2col load of A (128 pixels x
+//               BK channels of one filter tap, zero-filled at the borders) and
+//               one tiled load of B (BN output channels x BK channels of that
+//               tap) into a STAGES-deep shared-memory ring; no im2col buffer
+//               ever exists in global memory.
+//   warp 1      MMA issuer: tcgen05.mma (M=128, N=BN, K=16) into a TMEM
+//               accumulator; two accumulators so the epilogue of tile i
+//               overlaps the K loop of tile i+1.
+//   warps 4..7  epilogue ("The shape of it"): tcgen05.ld of the finished tile,
+//               acc*scale + bias, SiLU, bf16 cast, staged through swizzled
+//               shared memory and written by TMA stores.  x is read once and y
+//               written once; the conv result never goes to memory.
+// Every mbarrier wait is bounded in time; on timeout the kernel records an
+// error bit, waits for its own copies in flight, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "cbs_internal.h"
+#include "epilogue.cuh"
+#include "ptx.cuh"
+
+namespace cbs {
+
+__device__ unsigned int g_tc_error = 0;
+
+namespace {
+
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+
+struct TcArgs {
+    const float *scale;
+    const float *bias;
+    int c_out;
+    int m;  // output pixels
+    int n_tiles, tiles;
+    int howo, wo;
+    int stride_h, stride_w, pad_h, pad_w;
+    int s;
+    int c_chunks, k_iters;
+};
+
+template <int BN, int BK>
+struct TcCfg {
+    static constexpr int BM = kTcBlockM;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int A_STRIDE = (A_BYTES + 1023) / 1024 * 1024;
+    static constexpr int B_STRIDE = (B_BYTES + 1023) / 1024 * 1024;
+    static constexpr int EC = BN < 64 ? BN : 64;  // epilogue columns per chunk
+    static constexpr int STG_BYTES = 32 * EC * 2;  // one warp's staging buffer (32 rows)
+    static constexpr int STG_TOTAL = 4 * 2 * STG_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN;
+    static constexpr int ROW_A = BK * 2;  // operand row bytes = swizzle span
+    static constexpr int SMEM_LIMIT = 232448;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int STAGES_FIT =
+        (SMEM_LIMIT - 1024 - STG_TOTAL - BAR_BYTES) / (A_STRIDE + B_STRIDE);
+    static constexpr int STAGES = STAGES_FIT < 8 ? STAGES_FIT : 8;
+    static constexpr int SMEM = 1024 + STAGES * (A_STRIDE + B_STRIDE) + STG_TOTAL + BAR_BYTES;
+    static_assert(STAGES >= 2, "shared memory too small for two stages");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
+    static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 ||
+                      TMEM_COLS == 512,
+                  "TMEM allocation must be a power of two >= 32");
+};
+
+__device__ __forceinline__ void record_error(unsigned int bit, volatile int *abort_flag)
+{
+    atomicOr(&g_tc_error, bit);
+    *abort_flag = 1;
+}
+
+// XOR swizzle of a byte offset inside a 1024-byte aligned buffer whose rows
+// are `ROW` bytes (32/64/128), matching CU_TENSOR_MAP_SWIZZLE_{32,64,128}B.
+template <int ROW>
+__device__ __forceinline__ uint32_t swizzle_offset(uint32_t off)
+{
+    constexpr uint32_t mask = ROW == 128 ? 7u : (ROW == 64 ? 3u : 1u);
+    return off ^ (((off >> 7) & mask) << 4);
+}
+
+template <int BN, int BK>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_conv_bn_silu_kernel(const __grid_constant__ CUtensorMap tm_x,
+                           const __grid_constant__ CUtensorMap tm_w,
+                           const __grid_constant__ CUtensorMap tm_y, const TcArgs a)
+{
+    using C = TcCfg<BN, BK>;
+    constexpr int STAGES = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sm_a = smem;
+    uint8_t *sm_b = sm_a + STAGES * C::A_STRIDE;
+    uint8_t *sm_stg = sm_b + STAGES * C::B_STRIDE;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm_stg + C::STG_TOTAL);
+    uint64_t *full = bars;
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            dev::mbar_init(dev::smem_u32(&full[i]), 1);
+            dev::mbar_init(dev::smem_u32(&empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            dev::mbar_init(dev::smem_u32(&tfull[i]), 1);
+            dev::mbar_init(dev::smem_u32(&tempty[i]), 4);
+        }
+        dev::mbar_init(dev::smem_u32(drain), 1);
+        *abort_flag = 0;
+        dev::fence_mbarrier_init();
+    }
+    if (threadIdx.x == 32) {
+        dev::prefetch_tensormap(&tm_x);
+        dev::prefetch_tensormap(&tm_w);
+        dev::prefetch_tensormap(&tm_y);
+    }
+    if (warp == 1) {
+        dev::tmem_alloc(dev::smem_u32(tmem_slot), C::TMEM_COLS);
+        dev::tmem_relinquish_alloc_permit();
+    }
+    dev::tc_fence_before_sync();
+    __syncthreads();
+    dev::tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, issued_parity = 0;
+            for (int t = blockIdx.x; t < a.tiles && !*abort_flag; t += gridDim.x) {
+                const int m_tile = t / a.n_tiles;
+                const int n0 = (t - m_tile * a.n_tiles) * BN;
+                const int m0 = m_tile * C::BM;
+                const int img = m0 / a.howo;
+                const int rem = m0 - img * a.howo;
+                const int oh = rem / a.wo;
+                const int ow = rem - oh * a.wo;
+                const int corner_w = ow * a.stride_w - a.pad_w;
+                const int corner_h = oh * a.stride_h - a.pad_h;
+                int r = 0, s = 0, cc = 0;
+                bool ok = true;
+                for (int it = 0; it < a.k_iters; ++it) {
+                    const uint32_t e_bar = dev::smem_u32(&empty[stage]);
+                    if (!dev::mbar_wait_bounded(e_bar, phase ^ 1u, abort_flag, kWaitTimeoutNs)) {
+                        if (!*abort_flag) record_error(kErrTimeoutProducer, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t f_bar = dev::smem_u32(&full[stage]);
+                    dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES + C::B_BYTES);
+                    dev::tma_load_im2col_4d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_x, f_bar,
+                                            cc * BK, corner_w, corner_h, img, (uint16_t)s,
+                                            (uint16_t)r);
+                    dev::tma_load_3d(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f_bar,
+                                     cc * BK, r * a.s + s, n0);
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++cc == a.c_chunks) {
+                        cc = 0;
+                        if (++s == a.s) {
+                            s = 0;
+                            ++r;
+                        }
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+            }
+            // Every load issued must land before the CTA may exit.
+            for (int i = 0; i < STAGES; ++i) {
+                if ((issued >> i) & 1u) {
+                    if (!dev::mbar_wait_bounded(dev::smem_u32(&full[i]), (issued_parity >> i) & 1u,
+                                                nullptr, kWaitTimeoutNs))
+                        record_error(kErrTimeoutDrain, abort_flag);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = dev::idesc_bf16_f32(C::BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int lt = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < a.tiles && ok; t += gridDim.x, ++lt) {
+                const int buf = lt & 1;
+                const uint32_t tparity = (uint32_t)(lt >> 1) & 1u;
+                if (!dev::mbar_wait_bounded(dev::smem_u32(&tempty[buf]), tparity ^ 1u, abort_flag,
+                                            kWaitTimeoutNs)) {
+                    if (!*abort_flag) record_error(kErrTimeoutMma, abort_flag);
+                    break;
+                }
+                dev::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                for (int it = 0; it < a.k_iters; ++it) {
+                    if (!dev::mbar_wait_bounded(dev::smem_u32(&full[stage]), phase, abort_flag,
+                                                kWaitTimeoutNs)) {
+                        if (!*abort_flag) record_error(kErrTimeoutMma, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    dev::tc_fence_after_sync();
+                    const uint32_t a_addr = dev::smem_u32(sm_a + stage * C::A_STRIDE);
+                    const uint32_t b_addr = dev::smem_u32(sm_b + stage * C::B_STRIDE);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t da = dev::smem_desc_kmajor(a_addr + kk * 32, C::ROW_A);
+                        const uint64_t db = dev::smem_desc_kmajor(b_addr + kk * 32, C::ROW_A);
+                        dev::tc_mma_bf16(d_tmem, da, db, idesc, (it | kk) != 0 ? 1u : 0u);
+                    }
+                    dev::tc_commit(dev::smem_u32(&empty[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                dev::tc_commit(dev::smem_u32(&tfull[buf]));
+            }
+            // All MMAs issued by this thread must finish before TMEM is freed.
+            dev::tc_commit(dev::smem_u32(drain));
+            if (!dev::mbar_wait_bounded(dev::smem_u32(drain), 0, nullptr, kWaitTimeoutNs))
+                record_error(kErrTimeoutDrain, abort_flag);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        constexpr int EC = C::EC;
+        constexpr int ROW_Y = EC * 2;
+        const int ew = warp & 3;  // this warp may access TMEM lanes [32*ew, 32*ew+32)
+        uint8_t *my_stg = sm_stg + ew * 2 * C::STG_BYTES;
+        int sbuf = 0;
+        int lt = 0;
+        for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++lt) {
+            const int buf = lt & 1;
+            const uint32_t tparity = (uint32_t)(lt >> 1) & 1u;
+            int ok = 1;
+            if (lane == 0)
+                ok = dev::mbar_wait_bounded(dev::smem_u32(&tfull[buf]), tparity, abort_flag,
+                                            kWaitTimeoutNs)
+                         ? 1
+                         : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0 && !*abort_flag) record_error(kErrTimeoutEpilogue, abort_flag);
+                break;
+            }
+            dev::tc_fence_after_sync();
+            const int m_tile = t / a.n_tiles;
+            const int n0 = (t - m_tile * a.n_tiles) * BN;
+            const int row0 = m_tile * C::BM + ew * 32;  // first output pixel of this warp
+            const uint32_t t_lane = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN);
+#pragma unroll 1
+            for (int j = 0; j < BN / EC; ++j) {
+                uint32_t v[EC];
+#pragma unroll
+                for (int q = 0; q < EC / 16; ++q)
+                    dev::tmem_ld_32x32b_x16(t_lane + (uint32_t)(j * EC + q * 16), v + q * 16);
+                dev::tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < EC / 16; ++q) dev::reg_fence16(v + q * 16);
+                if (j == BN / EC - 1) {
+                    // The accumulator is in registers: hand the TMEM buffer back to the MMA warp.
+                    dev::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
+                }
+                const int ch0 = n0 + j * EC;
+                uint32_t packed[EC / 2];
+                if (ch0 + EC <= a.c_out) {
+#pragma unroll
+                    for (int i = 0; i < EC; i += 4) {
+                        const float4 sc = __ldg(reinterpret_cast<const float4 *>(a.scale + ch0 + i));
+                        const float4 bi = __ldg(reinterpret_cast<const float4 *>(a.bias + ch0 + i));
+                        packed[i / 2] = dev::pack_bf16x2(dev::bn_silu(__uint_as_float(v[i]), sc.x, bi.x),
+                                                         dev::bn_silu(__uint_as_float(v[i + 1]), sc.y, bi.y));
+                        packed[i / 2 + 1] =
+                            dev::pack_bf16x2(dev::bn_silu(__uint_as_float(v[i + 2]), sc.z, bi.z),
+                                             dev::bn_silu(__uint_as_float(v[i + 3]), sc.w, bi.w));
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < EC; i += 2) {
+                        const int c0 = ch0 + i, c1 = ch0 + i + 1;
+                        const float s0 = c0 < a.c_out ? __ldg(a.scale + c0) : 0.f;
+                        const float b0 = c0 < a.c_out ? __ldg(a.bias + c0) : 0.f;
+                        const float s1 = c1 < a.c_out ? __ldg(a.scale + c1) : 0.f;
+                        const float b1 = c1 < a.c_out ? __ldg(a.bias + c1) : 0.f;
+                        packed[i / 2] = dev::pack_bf16x2(dev::bn_silu(__uint_as_float(v[i]), s0, b0),
+                                                         dev::bn_silu(__uint_as_float(v[i + 1]), s1, b1));
+                    }
+                }
+                // Stage the warp's 32 rows x EC channels, then one TMA store.
+                if (lane == 0) dev::bulk_wait_group_read<1>();
+                __syncwarp();
+                uint8_t *sb = my_stg + sbuf * C::STG_BYTES;
+#pragma unroll
+                for (int q = 0; q < ROW_Y / 16; ++q) {
+                    const uint32_t off = swizzle_offset<ROW_Y>((uint32_t)(lane * ROW_Y + q * 16));
+                    *reinterpret_cast<uint4 *>(sb + off) =
+                        make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                }
+                dev::fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0 && row0 < a.m && ch0 < a.c_out) {
+                    dev::tma_store_2d(&tm_y, dev::smem_u32(sb), ch0, row0);
+                    dev::bulk_commit_group();
+                }
+                sbuf ^= 1;
+            }
+        }
+        if (lane == 0) dev::bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    dev::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        dev::tc_fence_after_sync();
+        dev::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+PFN_cuTensorMapEncodeIm2col_v12000 g_encode_im2col = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_status = cudaSuccess;
+
+cudaError_t load_encoders()
+{
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q1, q2;
+        void *f1 = nullptr, *f2 = nullptr;
+        cudaError_t e1 = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f1, 12000,
+                                                          cudaEnableDefault, &q1);
+        cudaError_t e2 = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &f2, 12000,
+                                                          cudaEnableDefault, &q2);
+        if (e1 != cudaSuccess || e2 != cudaSuccess || q1 != cudaDriverEntryPointSuccess ||
+            q2 != cudaDriverEntryPointSuccess || !f1 || !f2) {
+            g_encode_status = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : cudaErrorNotSupported);
+            return;
+        }
+        g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f1);
+        g_encode_im2col = reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(f2);
+    });
+    return g_encode_status;
+}
+
+CUtensorMapSwizzle swizzle_for_row_bytes(int row_bytes)
+{
+    return row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                            : (row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+struct TcMaps {
+    CUtensorMap x, w, y;
+};
+
+cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, TcMaps *maps)
+{
+    cudaError_t st = load_encoders();
+    if (st != cudaSuccess) return st;
+    const CUtensorMapSwizzle sw_k = swizzle_for_row_bytes(block_k * 2);
+    // x: im2col view over (C, W, H, N).  The bounding box of window corners is
+    // [-pad, dim - 1 + pad - (filter - 1)] along W and H, traversed with the
+    // convolution stride, so a box of 128 pixels walks output pixels in
+    // (img, oh, ow) order, crossing rows and images.
+    {
+        cuuint64_t dims[4] = {(cuuint64_t)p.c, (cuuint64_t)p.w_in, (cuuint64_t)p.h, (cuuint64_t)p.n};
+        cuuint64_t strides[3] = {(cuuint64_t)p.c * 2, (cuuint64_t)p.w_in * p.c * 2,
+                                 (cuuint64_t)p.h * p.w_in * p.c * 2};
+        int lower[2] = {-p.pad_w, -p.pad_h};
+        int upper[2] = {p.pad_w - (p.s - 1), p.pad_h - (p.r - 1)};
+        cuuint32_t estr[4] = {1, (cuuint32_t)p.stride_w, (cuuint32_t)p.stride_h, 1};
+        CUresult r = g_encode_im2col(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(p.x),
+                                     dims, strides, lower, upper, (cuuint32_t)block_k,
+                                     (cuuint32_t)kTcBlockM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw_k,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    // W: (C, R*S, C_out), box (BK, 1, BN).
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)p.c, (cuuint64_t)p.r * p.s, (cuuint64_t)p.c_out};
+        cuuint64_t strides[2] = {(cuuint64_t)p.c * 2, (cuuint64_t)p.r * p.s * p.c * 2};
+        cuuint32_t box[3] = {(cuuint32_t)block_k, 1, (cuuint32_t)block_n};
+        cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = g_encode_tiled(&maps->w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.w),
+                                    dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw_k,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    // y: (C_out, M), box (EC, 32): one epilogue warp's rows.
+    {
+        const int ec = block_n < 64 ? block_n : 64;
+        cuuint64_t dims[2] = {(cuuint64_t)p.c_out, (cuuint64_t)p.m};
+        cuuint64_t strides[1] = {(cuuint64_t)p.c_out * 2};
+        cuuint32_t box[2] = {(cuuint32_t)ec, 32};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = g_encode_tiled(&maps->y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.y, dims, strides,
+                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                    swizzle_for_row_bytes(ec * 2), CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
+// Encoded tensor maps of recent calls, keyed by pointers, shape and tile.  Encoding
+// is a driver call; layers called repeatedly on the same buffers reuse it.
+struct MapKey {
+    const void *x, *w, *y;
+    int dims[11];
+    int block_n, block_k, device;
+    bool operator==(const MapKey &o) const
+    {
+        if (x != o.x || w != o.w || y != o.y || block_n != o.block_n || block_k != o.block_k ||
+            device != o.device)
+            return false;
+        for (int i = 0; i < 11; ++i)
+            if (dims[i] != o.dims[i]) return false;
+        return true;
+    }
+};
+
+struct MapCache {
+    static constexpr int kSlots = 64;
+    std::mutex mu;
+    MapKey keys[kSlots];
+    TcMaps maps[kSlots];
+    bool used[kSlots] = {};
+    int next = 0;
+};
+
+MapCache g_map_cache;
+
+cudaError_t cached_maps(const ConvProblem &p, int block_n, int block_k, TcMaps *out)
+{
+    MapKey k{};
+    k.x = p.x;
+    k.w = p.w;
+    k.y = p.y;
+    const int d[11] = {p.n, p.h, p.w_in, p.c, p.c_out, p.r, p.s, p.stride_h, p.stride_w, p.pad_h, p.pad_w};
+    for (int i = 0; i < 11; ++i) k.dims[i] = d[i];
+    k.block_n = block_n;
+    k.block_k = block_k;
+    cudaError_t st = cudaGetDevice(&k.device);
+    if (st != cudaSuccess) return st;
+    {
+        std::lock_guard<std::mutex> lock(g_map_cache.mu);
+        for (int i = 0; i < MapCache::kSlots; ++i) {
+            if (g_map_cache.used[i] && g_map_cache.keys[i] == k) {
+                *out = g_map_cache.maps[i];
+                return cudaSuccess;
+            }
+        }
+    }
+    st = encode_maps(p, block_n, block_k, out);
+    if (st != cudaSuccess) return st;
+    std::lock_guard<std::mutex> lock(g_map_cache.mu);
+    const int slot = g_map_cache.next;
+    g_map_cache.next = (slot + 1) % MapCache::kSlots;
+    g_map_cache.keys[slot] = k;
+    g_map_cache.maps[slot] = *out;
+    g_map_cache.used[slot] = true;
+    return cudaSuccess;
+}
+
+template <int BN, int BK>
+cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &maps, cudaStream_t stream)
+{
+    using C = TcCfg<BN, BK>;
+    auto kern = tc_conv_bn_silu_kernel<BN, BK>;
+    // The shared-memory opt-in is per function and device: done once per device.
+    static std::mutex attr_mu;
+    static unsigned long long attr_done = 0;  // bit per device ordinal (< 64)
+    int device = 0;
+    cudaError_t st = cudaGetDevice(&device);
+    if (st != cudaSuccess) return st;
+    {
+        std::lock_guard<std::mutex> lock(attr_mu);
+        const unsigned long long bit = device < 64 ? (1ull << device) : 0ull;
+        if (!(attr_done & bit) || bit == 0) {
+            st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+            if (st != cudaSuccess) return st;
+            attr_done |= bit;
+        }
+    }
+    TcArgs a;
+    a.scale = p.scale;
+    a.bias = p.bias;
+    a.c_out = p.c_out;
+    a.m = (int)p.m;
+    a.n_tiles = plan.n_tiles;
+    a.tiles = plan.tiles;
+    a.howo = p.ho * p.wo;
+    a.wo = p.wo;
+    a.stride_h = p.stride_h;
+    a.stride_w = p.stride_w;
+    a.pad_h = p.pad_h;
+    a.pad_w = p.pad_w;
+    a.s = p.s;
+    a.c_chunks = plan.c_chunks;
+    a.k_iters = plan.k_iters;
+    kern<<<plan.grid, kTcThreads, C::SMEM, stream>>>(maps.x, maps.w, maps.y, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_smem_bytes(int block_n, int block_k, int stages)
+{
+    const int a = (kTcBlockM * block_k * 2 + 1023) / 1024 * 1024;
+    const int b = (block_n * block_k * 2 + 1023) / 1024 * 1024;
+    const int ec = block_n < 64 ? block_n : 64;
+    return 1024 + stages * (a + b) + 8 * 32 * ec * 2 + 256;
+}
+
+static int stages_for(int block_n, int block_k)
+{
+    const int a = (kTcBlockM * block_k * 2 + 1023) / 1024 * 1024;
+    const int b = (block_n * block_k * 2 + 1023) / 1024 * 1024;
+    const int ec = block_n < 64 ? block_n : 64;
+    const int fit = (232448 - 1024 - 8 * 32 * ec * 2 - 256) / (a + b);
+    return fit < 8 ? fit : 8;
+}
+
+bool tc_supported(const ConvProblem &p)
+{
+    // TMA needs 16-byte row strides (c % 8, c_out % 8) and the channel chunk of
+    // one K step must be one swizzle span of 32/64/128 bytes (c % 16).  The
+    // im2col box corners are limited to [-128, 127]; the GEMM row count to int.
+    if (p.c % 16 != 0 || p.c_out % 8 != 0) return false;
+    // Square filters with equal stride and padding on both axes only, so the
+    // im2col box corners are the same along W and H.
+    if (p.r != p.s || p.stride_h != p.stride_w || p.pad_h != p.pad_w) return false;
+    if (p.pad_h > 127 || p.pad_w > 127 || p.r - 1 - p.pad_h > 128 || p.s - 1 - p.pad_w > 128) return false;
+    if (p.stride_h > 8 || p.stride_w > 8) return false;
+    if (p.m > 0x7fffffffLL - kTcBlockM) return false;
+    return true;
+}
+
+TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
+{
+    TcPlan t{};
+    t.block_k = p.c % 64 == 0 ? 64 : (p.c % 32 == 0 ? 32 : 16);
+    const int m_tiles = (int)((p.m + kTcBlockM - 1) / kTcBlockM);
+    if (p.c_out <= 128) {
+        t.block_n = p.c_out <= 16 ? 16 : (p.c_out <= 32 ? 32 : (p.c_out <= 64 ? 64 : 128));
+    } else {
+        // Choose 128 or 256 output channels per tile by the estimated number of
+        // waves times the per-tile work (which scales with the tile width).
+        long long best = -1;
+        for (int bn : {256, 128}) {
+            const long long tiles = (long long)m_tiles * ((p.c_out + bn - 1) / bn);
+            const long long waves = (tiles + sm_count - 1) / sm_count;
+            const long long cost = waves * bn;
+            if (best < 0 || cost < best) {
+                best = cost;
+                t.block_n = bn;
+            }
+        }
+    }
+    t.stages = stages_for(t.block_n, t.block_k);
+    t.c_chunks = (p.c + t.block_k - 1) / t.block_k;
+    t.k_iters = p.r * p.s * t.c_chunks;
+    t.m_tiles = m_tiles;
+    t.n_tiles = (p.c_out + t.block_n - 1) / t.block_n;
+    t.tiles = t.m_tiles * t.n_tiles;
+    t.grid = std::min(t.tiles, sm_count);
+    t.smem_bytes = tc_smem_bytes(t.block_n, t.block_k, t.stages);
+    return t;
+}
+
+cudaError_t tc_launch(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream)
+{
+    TcMaps maps;
+    cudaError_t st = cached_maps(p, plan.block_n, plan.block_k, &maps);
+    if (st != cudaSuccess) return st;
+#define CBS_TC_CASE(BN_, BK_) \
+    if (plan.block_n == BN_ && plan.block_k == BK_) return launch_cfg<BN_, BK_>(p, plan, maps, stream);
+    CBS_TC_CASE(16, 16) CBS_TC_CASE(16, 32) CBS_TC_CASE(16, 64)
+    CBS_TC_CASE(32, 16) CBS_TC_CASE(32, 32) CBS_TC_CASE(32, 64)
+    CBS_TC_CASE(64, 16) CBS_TC_CASE(64, 32) CBS_TC_CASE(64, 64)
+    CBS_TC_CASE(128, 16) CBS_TC_CASE(128, 32) CBS_TC_CASE(128, 64)
+    CBS_TC_CASE(256, 16) CBS_TC_CASE(256, 32) CBS_TC_CASE(256, 64)
+#undef CBS_TC_CASE
+    return cudaErrorInvalidConfiguration;
+}
+
+cudaError_t tc_read_and_clear_error(cudaStream_t stream, unsigned int *out)
+{
+    unsigned int host = 0;
+    cudaError_t st = cudaMemcpyFromSymbolAsync(&host, g_tc_error, sizeof host, 0,
+                                               cudaMemcpyDeviceToHost, stream);
+    if (st == cudaSuccess) st = cudaStreamSynchronize(stream);
+    if (st != cudaSuccess) return st;
+    if (host != 0) {
+        const unsigned int zero = 0;
+        st = cudaMemcpyToSymbolAsync(g_tc_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, stream);
+        if (st == cudaSuccess) st = cudaStreamSynchronize(stream);
+    }
+    *out = host;
+    return st;
+}
+
+}  // namespace cbs

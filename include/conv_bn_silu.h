@@ -1,0 +1,139 @@
+/*
+ * conv_bn_silu.h -- C ABI of the fused conv2d -> BatchNorm -> SiLU layer for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer computes, per output pixel and output channel k,
+ *
+ *     y = SiLU(conv2d(x, W) * scale[k] + bias[k]),   SiLU(z) = z * sigmoid(z),
+ *
+ * as one kernel that reads x once and writes y once: the BatchNorm multiply/add
+ * and the SiLU are applied to the convolution's output tile while it is still
+ * on chip ("Fusing an Epilogue", kernels book, sections "The problem",
+ * "What an epilogue is" and "The shape of it").
+ *
+ * Conventions shared by every entry point:
+ *   - Layouts: x is NHWC [n][h][w][c] bf16; W is KRSC [c_out][r][s][c] bf16
+ *     (for each output channel, the filter taps row by row, channels
+ *     innermost); y is NHWC [n][ho][wo][c_out] bf16; every tensor dense.
+ *   - The convolution is a cross-correlation with zero padding, dilation 1 and
+ *     groups 1; ho = (h + 2*pad_h - r)/stride_h + 1 (floor), likewise wo.
+ *   - Pointers named device are CUDA device (or managed) memory owned by the
+ *     caller.  The library keeps no reference to them after a call returns and
+ *     never frees or reallocates them.  Inputs are never written.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous: they validate, enqueue and return.
+ *   - Every function returns a cbs_status.  Invalid arguments return an error
+ *     without launching anything.  A fault inside a kernel surfaces at the
+ *     caller's next synchronisation, like any CUDA launch; a pipeline wait
+ *     that exceeded its time bound inside a kernel is reported by
+ *     conv_bn_silu_check().
+ *   - Thread safety: all entry points may be called from several host threads.
+ */
+#ifndef CONV_BN_SILU_H
+#define CONV_BN_SILU_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum cbs_status {
+    CBS_OK = 0,
+    CBS_ERR_INVALID_ARG = 1, /* null pointer, dim <= 0, stride < 1, pad < 0, ho/wo < 1, eps < 0 */
+    CBS_ERR_MISALIGNED = 2,  /* a device pointer is not 16-byte aligned */
+    CBS_ERR_UNSUPPORTED = 3, /* the requested algorithm cannot run this shape */
+    CBS_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed; see conv_bn_silu_last_cuda_error() */
+    CBS_ERR_TIMEOUT = 5      /* a kernel's pipeline wait ran past its bound and the kernel gave up */
+} cbs_status;
+
+/* Kernel choice for conv_bn_silu_forward_algo(). */
+typedef enum cbs_algo {
+    CBS_ALGO_AUTO = 0,    /* pick by shape (what conv_bn_silu_forward does) */
+    CBS_ALGO_TCGEN05 = 1, /* implicit GEMM on the tcgen05 tensor cores, TMA-fed, TMEM accumulator */
+    CBS_ALGO_DIRECT = 2   /* CUDA-core direct convolution, one output pixel per thread; any shape */
+} cbs_algo;
+
+/*
+ * BatchNorm fold, run once per layer at load time.
+ *   scale[k] = gamma[k] / sqrt(var[k] + eps),  bias[k] = beta[k] - mean[k] * scale[k]
+ * The fusion page describes BN as "a multiply and an add" with "one scale and
+ * one bias per output channel" ("Fusing an Epilogue", sections "The problem"
+ * and "The shape of it"); this is the inference-mode fold with running
+ * statistics.  Computed in double precision, rounded once to float.
+ *   gamma, beta, mean, var : device, float32 [c_out]
+ *   eps                    : >= 0 and finite
+ *   scale, bias            : device, float32 [c_out], written; must not overlap the inputs
+ * c_out == 0 is a no-op.  var + eps <= 0 yields NaN/Inf in scale (not checked).
+ */
+int conv_bn_silu_fold(const float *gamma, const float *beta, const float *mean, const float *var,
+                      float eps, int c_out, float *scale, float *bias, void *stream);
+
+/*
+ * Fused forward pass: y = SiLU(conv2d(x, W) * scale + bias).
+ * ("Fusing an Epilogue", section "The shape of it": the K loop accumulates
+ * the output tile, then acc = acc*bn_scale + bn_bias, acc = acc*sigmoid(acc),
+ * then one store; section "Three kernels for one operation": convolution as
+ * a GEMM on the tensor cores.)
+ *   x     : device, bf16 NHWC [n][h][w_in][c]
+ *   w     : device, bf16 KRSC [c_out][r][s][c]
+ *   scale : device, float32 [c_out]  (from conv_bn_silu_fold, or any per-channel multiplier)
+ *   bias  : device, float32 [c_out]
+ *   y     : device, bf16 NHWC [n][ho][wo][c_out], written; must not overlap x, w, scale or bias
+ * All device pointers must be 16-byte aligned.  n == 0 or c_out == 0 is a
+ * no-op.  The result is bf16 rounded to nearest even from an fp32
+ * accumulator; it is deterministic (no atomics, fixed reduction order).
+ * Kernels: the tcgen05 implicit GEMM when c % 16 == 0 and c_out % 8 == 0,
+ * otherwise the CUDA-core direct kernel.
+ */
+int conv_bn_silu_forward(const void *x, const void *w, const float *scale, const float *bias,
+                         void *y, int n, int h, int w_in, int c, int c_out, int r, int s,
+                         int stride_h, int stride_w, int pad_h, int pad_w, void *stream);
+
+/* As conv_bn_silu_forward, with the kernel chosen by `algo` (a cbs_algo).
+ * Returns CBS_ERR_UNSUPPORTED when that kernel cannot run this shape. */
+int conv_bn_silu_forward_algo(const void *x, const void *w, const float *scale, const float *bias,
+                              void *y, int n, int h, int w_in, int c, int c_out, int r, int s,
+                              int stride_h, int stride_w, int pad_h, int pad_w, int algo,
+                              void *stream);
+
+/* Output spatial size of the convolution; host only, touches no GPU.
+ * ho = (h + 2*pad_h - r)/stride_h + 1, wo likewise; CBS_ERR_INVALID_ARG when
+ * either would be < 1 or an argument is out of range. */
+int conv_bn_silu_output_dims(int h, int w_in, int r, int s, int stride_h, int stride_w,
+                             int pad_h, int pad_w, int *ho, int *wo);
+
+/* What conv_bn_silu_forward_algo would launch for this shape; host only. */
+typedef struct cbs_plan_info {
+    int algo;         /* cbs_algo actually selected (never CBS_ALGO_AUTO) */
+    int block_m;      /* output pixels per tile */
+    int block_n;      /* output channels per tile */
+    int block_k;      /* reduction depth (channels) per pipeline stage */
+    int stages;       /* shared-memory pipeline depth (0 for the direct kernel) */
+    int tiles;        /* output tiles */
+    int grid;         /* CTAs launched */
+    int threads;      /* threads per CTA */
+    int smem_bytes;   /* dynamic shared memory per CTA */
+    int k_iters;      /* pipeline steps per tile */
+} cbs_plan_info;
+
+/* Fills `info` for the given shape, algorithm and SM count (sm_count > 0;
+ * pass the device's multiprocessor count).  Host only, touches no GPU. */
+int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, int stride_h,
+                      int stride_w, int pad_h, int pad_w, int algo, int sm_count,
+                      cbs_plan_info *info);
+
+/* Synchronises `stream`, then reads and clears the library's device error word.
+ * Returns CBS_ERR_TIMEOUT if any kernel since the last check gave up on a
+ * pipeline wait, CBS_ERR_CUDA if the synchronisation failed, else CBS_OK. */
+int conv_bn_silu_check(void *stream);
+
+/* Short English text for a cbs_status value (static storage, never NULL). */
+const char *conv_bn_silu_status_string(int status);
+
+/* The cudaError_t behind the calling thread's most recent CBS_ERR_CUDA (0 if none). */
+int conv_bn_silu_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV_BN_SILU_H */

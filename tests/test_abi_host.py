@@ -1,0 +1,130 @@
+"""The C-ABI library on the host, without a GPU.
+
+Checks that libconvbnsilu.so builds, loads and exports every function that
+include/*.h declares, and exercises the entry points that touch no GPU:
+output sizes, the tile planner, and argument validation (every invalid call
+must return its status code before any CUDA call is made).
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from conv2d_batchnorm_silu_gb300 import _build
+    _build.build()
+    from conv2d_batchnorm_silu_gb300 import capi
+    return capi
+
+
+def declared_functions():
+    names = []
+    for hdr in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(hdr).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                             text, flags=re.M):
+            if m.group(1) not in ("if", "return", "sizeof"):
+                names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("conv_bn_silu_fold", "conv_bn_silu_forward", "conv_bn_silu_output_dims"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, missing
+
+
+def test_output_dims(lib):
+    assert lib.output_dims(640, 640, 3, 3, 2, 1) == (320, 320)
+    assert lib.output_dims(160, 160, 3, 3, 2, 1) == (80, 80)
+    assert lib.output_dims(40, 40, 1, 1, 1, 0) == (40, 40)
+    assert lib.output_dims(20, 20, 3, 3, 1, 1) == (20, 20)
+    assert lib.output_dims(7, 9, 3, 2, (2, 3), (0, 1)) == (3, 4)
+    assert lib.output_dims(1, 1, 3, 3, 1, 1) == (1, 1)
+    for bad in [(0, 5, 1, 1, 1, 0), (5, 5, 3, 3, 0, 0), (5, 5, 3, 3, 1, -1), (2, 2, 3, 3, 1, 0)]:
+        with pytest.raises(lib.CbsError):
+            lib.output_dims(*bad)
+
+
+def test_plan_for_the_five_layers(lib):
+    from conv2d_batchnorm_silu_gb300.synthetic import LAYERS
+    expect_algo = {"tiny": "tcgen05", "stem": "direct", "down": "tcgen05",
+                   "pointwise": "tcgen05", "deep": "tcgen05"}
+    for name, sh in LAYERS.items():
+        p = lib.plan(sh.n, sh.h, sh.w, sh.c, sh.k, sh.r, sh.s, sh.stride, sh.pad, "auto", 152)
+        assert p["algo"] == expect_algo[name], (name, p)
+        if p["algo"] == "tcgen05":
+            assert p["block_m"] == 128 and p["block_n"] % 16 == 0 and p["block_n"] <= 256
+            assert p["block_n"] >= min(sh.k, 128)
+            assert p["grid"] <= 152 and p["grid"] <= p["tiles"]
+            assert p["smem_bytes"] <= 232448
+            assert p["stages"] >= 2
+            assert p["k_iters"] == sh.r * sh.s * -(-sh.c // p["block_k"])
+            tiles = -(-sh.m // 128) * -(-sh.k // p["block_n"])
+            assert p["tiles"] == tiles
+
+
+def test_plan_rejects_what_tcgen05_cannot_run(lib):
+    with pytest.raises(lib.CbsError) as e:
+        lib.plan(1, 64, 64, 3, 16, 3, 3, 2, 1, "tcgen05", 152)   # c = 3: 6-byte pixel stride
+    assert e.value.status == lib.CBS_ERR_UNSUPPORTED
+    with pytest.raises(lib.CbsError):
+        lib.plan(1, 64, 64, 16, 12, 3, 3, 1, 1, "tcgen05", 152)  # c_out % 8 != 0
+    assert lib.plan(1, 64, 64, 3, 16, 3, 3, 2, 1, "direct", 152)["algo"] == "direct"
+
+
+def test_invalid_arguments_return_status_without_gpu(lib):
+    f = lib.raw_status
+    P = ctypes.c_void_p
+    good = P(0x10000)
+    odd = P(0x10008)
+    # null pointer
+    assert f("conv_bn_silu_forward", None, good, good, good, good, 1, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1,
+             None) == lib.CBS_ERR_INVALID_ARG
+    # misaligned pointer
+    assert f("conv_bn_silu_forward", good, odd, good, good, good, 1, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1,
+             None) == lib.CBS_ERR_MISALIGNED
+    # bad dims / stride / pad / kernel larger than padded input
+    for dims in [(1, 0, 8, 16, 16, 3, 3, 1, 1, 1, 1), (1, 8, 8, 0, 16, 3, 3, 1, 1, 1, 1),
+                 (1, 8, 8, 16, 16, 3, 3, 0, 1, 1, 1), (1, 8, 8, 16, 16, 3, 3, 1, 1, -1, 1),
+                 (1, 2, 2, 16, 16, 5, 5, 1, 1, 0, 0), (-1, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1)]:
+        assert f("conv_bn_silu_forward", good, good, good, good, good, *dims, None) == \
+            lib.CBS_ERR_INVALID_ARG
+    # bad algorithm id
+    assert f("conv_bn_silu_forward_algo", good, good, good, good, good, 1, 8, 8, 16, 16, 3, 3, 1, 1,
+             1, 1, 7, None) == lib.CBS_ERR_INVALID_ARG
+    # unsupported shape for a forced tcgen05 call, rejected before any launch
+    assert f("conv_bn_silu_forward_algo", good, good, good, good, good, 1, 8, 8, 3, 16, 3, 3, 1, 1,
+             1, 1, 1, None) == lib.CBS_ERR_UNSUPPORTED
+    # empty batch / no output channels are no-ops even with null pointers
+    assert f("conv_bn_silu_forward", None, None, None, None, None, 0, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1,
+             None) == lib.CBS_OK
+    assert f("conv_bn_silu_forward", None, None, None, None, None, 2, 8, 8, 16, 0, 3, 3, 1, 1, 1, 1,
+             None) == lib.CBS_OK
+    # fold: negative eps, null pointers, misaligned, c_out == 0
+    fold = lib._lib.conv_bn_silu_fold
+    assert fold(good, good, good, good, -1.0, 4, good, good, None) == lib.CBS_ERR_INVALID_ARG
+    assert fold(good, None, good, good, 1e-3, 4, good, good, None) == lib.CBS_ERR_INVALID_ARG
+    assert fold(good, good, odd, good, 1e-3, 4, good, good, None) == lib.CBS_ERR_MISALIGNED
+    assert fold(None, None, None, None, 1e-3, 0, None, None, None) == lib.CBS_OK
+    assert fold(good, good, good, good, float("nan"), 4, good, good, None) == lib.CBS_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        assert isinstance(lib._status_string(st), bytes) and lib._status_string(st)
+    assert lib._status_string(99) == b"unknown status"
