@@ -13,9 +13,13 @@ Timing: W warm-up steps, then K steps between two CUDA events on the
 launching stream, bracketed by a barrier and torch.cuda.synchronize() on
 both sides; max over ranks.  Inputs rotate over 3 buffer sets (about 426 MB
 touched per rotation, more than three times the 129 MB L2), so each step
-reads its data from HBM.  Per-kernel launch times come from CUDA events
-recorded around the forward calls inside the same timed region.  SM clocks
-and throttle reasons are sampled with nvidia-smi during the timed region.
+reads its data from HBM.  The step is replayed from CUDA graphs captured
+from the API calls (ten launches through Python per step would make the host
+the bottleneck); the dominant layer's forward is its own graph, so CUDA events
+on the stream bracket exactly that kernel inside the timed region.  Per-layer
+times in ``per_layer`` come from a separate pass with the L2 flushed before
+each call.  SM clocks and throttle reasons are sampled with nvidia-smi during
+the timed region.
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead
 (the reference arm; a bounded sample of the same workload per step).
@@ -52,7 +56,7 @@ WORKLOAD = ("five YOLO-shaped fused conv+BN+SiLU layers per step, each BN fold +
 DOMINANT = "deep"
 ROTATION = 3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-CLOCK_FIELDS = ("uuid,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_FIELDS = ("timestamp,uuid,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -67,7 +71,17 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--reference-budget-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args(argv)
+    ap.add_argument("--layers", default=",".join(LAYER_ORDER),
+                    help="comma-separated subset of layers in the step (default: all five)")
+    ap.add_argument("--iso-iters", type=int, default=30,
+                    help="calls per layer for the per-layer (L2-flushed) timings")
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="launch through the API each step instead of replaying CUDA graphs")
+    args = ap.parse_args(argv)
+    args.layers = tuple(n for n in LAYER_ORDER if n in args.layers.split(","))
+    if not args.layers:
+        ap.error("--layers selects no known layer")
+    return args
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -126,7 +140,7 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
-    def stop(self) -> dict | None:
+    def stop(self, t0: float | None = None, t1: float | None = None) -> dict | None:
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -135,25 +149,38 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        return summarize_clocks(out, self.uuid)
+        return summarize_clocks(out, self.uuid, t0, t1)
 
 
-def summarize_clocks(csv_text: str, uuid: str | None) -> dict | None:
+def summarize_clocks(csv_text: str, uuid: str | None, t0: float | None = None,
+                     t1: float | None = None) -> dict | None:
+    """Median SM clock, max clock and throttle reasons from nvidia-smi CSV samples.
+
+    Only samples whose timestamp falls in [t0, t1] (host wall time) count, when given.
+    """
+    import datetime
     sm, sm_max, power, reasons = [], [], [], set()
     names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
     for line in csv_text.splitlines():
         parts = [p.strip() for p in line.split(",")]
-        if len(parts) < 10:
+        if len(parts) < 11:
             continue
-        if uuid and uuid not in parts[0]:
+        if uuid and uuid not in parts[1]:
             continue
+        if t0 is not None and t1 is not None:
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if ts < t0 or ts > t1:
+                continue
         try:
-            sm.append(float(parts[2]))
-            sm_max.append(float(parts[3]))
-            power.append(float(parts[4]))
+            sm.append(float(parts[3]))
+            sm_max.append(float(parts[4]))
+            power.append(float(parts[5]))
         except ValueError:
             continue
-        for name, val in zip(names, parts[6:10]):
+        for name, val in zip(names, parts[7:11]):
             if val.lower() == "active":
                 reasons.add(name)
     if not sm:
@@ -220,92 +247,162 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     dist_init(world, True)
-    stream = torch.cuda.current_stream(dev)
-    inputs = {name: make_layer_inputs(LAYERS[name]) for name in LAYER_ORDER}
-    sets = [{name: LayerBuffers(inputs[name], dev) for name in LAYER_ORDER} for _ in range(ROTATION)]
-    flops_step = sum(LAYERS[n].flops for n in LAYER_ORDER)
-    launches_per_step = 2 * len(LAYER_ORDER)
+    layers = args.layers
+    dominant = DOMINANT if DOMINANT in layers else max(layers, key=lambda n: LAYERS[n].flops)
+    stream = torch.cuda.Stream(dev)
+    inputs = {name: make_layer_inputs(LAYERS[name]) for name in layers}
+    sets = [{name: LayerBuffers(inputs[name], dev) for name in layers} for _ in range(ROTATION)]
+    flops_step = sum(LAYERS[n].flops for n in layers)
+    launches_per_step = 2 * len(layers)
+
+    def fold_call(lb, strm):
+        capi.fold(lb.g, lb.b, lb.m, lb.v, lb.eps, lb.scale, lb.bias, stream=strm)
+
+    def forward_call(lb, strm):
+        sh = lb.shape
+        capi.forward(lb.x, lb.w, lb.scale, lb.bias, sh.stride, sh.pad, y=lb.y, stream=strm)
+
+    # The step in launch order, split around the dominant layer's forward so that
+    # CUDA events on the stream can bracket exactly that kernel.
+    def segments(bufs):
+        pre, post, dom, seen = [], [], None, False
+        for name in layers:
+            (post if seen else pre).append(lambda s, lb=bufs[name]: fold_call(lb, s))
+            if name == dominant:
+                seen = True
+                dom = (lambda s, lb=bufs[name]: forward_call(lb, s))
+            else:
+                (post if seen else pre).append(lambda s, lb=bufs[name]: forward_call(lb, s))
+        return pre, dom, post
+
+    # Warm up through the API (first calls encode tensor maps and set kernel attributes).
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            pre, dom, post = segments(sets[i % ROTATION])
+            for f in pre + [dom] + post:
+                f(stream)
+    torch.cuda.synchronize()
+    capi.check(stream)
+
+    # One CUDA graph per segment per buffer set.
+    plan = []
+    for i in range(ROTATION):
+        pre, dom, post = segments(sets[i])
+        parts = []
+        for calls in (pre, [dom], post):
+            if not calls:
+                parts.append(None)
+            elif args.no_graphs:
+                parts.append(calls)
+            else:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for f in calls:
+                        f(None)
+                parts.append(g)
+        plan.append(parts)
+    torch.cuda.synchronize()
+
+    def run_part(part):
+        if part is None:
+            return
+        if isinstance(part, list):
+            for f in part:
+                f(stream)
+        else:
+            part.replay()
 
     def step(i, ev=None):
-        bufs = sets[i % ROTATION]
-        for name in LAYER_ORDER:
-            lb = bufs[name]
-            sh = lb.shape
-            capi.fold(lb.g, lb.b, lb.m, lb.v, lb.eps, lb.scale, lb.bias, stream=stream)
-            if ev is not None:
-                ev[name][0].record(stream)
-            capi.forward(lb.x, lb.w, lb.scale, lb.bias, sh.stride, sh.pad, y=lb.y, stream=stream)
-            if ev is not None:
-                ev[name][1].record(stream)
+        pre, dom, post = plan[i % ROTATION]
+        run_part(pre)
+        if ev is not None:
+            ev[0].record(stream)
+        run_part(dom)
+        if ev is not None:
+            ev[1].record(stream)
+        run_part(post)
 
-    for i in range(args.warmup):
-        step(i)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
     torch.cuda.synchronize()
     capi.check(stream)
 
     K = args.steps
-    per_kernel = {name: ([torch.cuda.Event(enable_timing=True) for _ in range(K)],
-                         [torch.cuda.Event(enable_timing=True) for _ in range(K)])
-                  for name in LAYER_ORDER}
+    dom_ev = ([torch.cuda.Event(enable_timing=True) for _ in range(K)],
+              [torch.cuda.Event(enable_timing=True) for _ in range(K)])
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(device_uuid(local_rank))
-    time.sleep(0.3)  # let the sampler start
+    time.sleep(0.5)  # let the sampler start
     barrier(world)
     torch.cuda.synchronize()
-    start.record(stream)
-    for i in range(K):
-        step(i, {n: (per_kernel[n][0][i], per_kernel[n][1][i]) for n in LAYER_ORDER})
-    end.record(stream)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(K):
+            step(i, (dom_ev[0][i], dom_ev[1][i]))
+        end.record(stream)
     torch.cuda.synchronize()
+    t_wall1 = time.time()
     barrier(world)
-    clocks = sampler.stop()
+    clocks = sampler.stop(t_wall0, t_wall1)
     capi.check(stream)
     elapsed_s = start.elapsed_time(end) / 1e3
     elapsed_max = max_over_ranks(elapsed_s, world, dev)
-    per_layer_us = {n: 1e3 * float(np.mean([a.elapsed_time(b) for a, b in zip(*per_kernel[n])]))
-                    for n in LAYER_ORDER}
+    dom_us = 1e3 * float(np.mean([a.elapsed_time(b) for a, b in zip(*dom_ev)]))
 
     peaks, peak_src = load_peaks()
+    iso = isolated_layer_times(capi, sets, layers, stream, dev, args.iso_iters)
     per_layer = {}
-    for n in LAYER_ORDER:
+    for n in layers:
         sh = LAYERS[n]
-        t = per_layer_us[n] * 1e-6
-        roof = max(sh.flops / (peaks["bf16_tflops"] * 1e12), sh.compulsory_bytes / (peaks["hbm_gbs"] * 1e9))
-        plan = capi.plan(sh.n, sh.h, sh.w, sh.c, sh.k, sh.r, sh.s, sh.stride, sh.pad)
-        per_layer[n] = {"us_per_call": round(per_layer_us[n], 3),
+        t = iso[n] * 1e-6
+        t_flop = sh.flops / (peaks["bf16_tflops"] * 1e12)
+        t_byte = sh.compulsory_bytes / (peaks["hbm_gbs"] * 1e9)
+        pl = capi.plan(sh.n, sh.h, sh.w, sh.c, sh.k, sh.r, sh.s, sh.stride, sh.pad)
+        per_layer[n] = {"us_per_call": round(iso[n], 3),
                         "tflops": round(sh.flops / t / 1e12, 2),
                         "gbs": round(sh.compulsory_bytes / t / 1e9, 1),
-                        "roofline_us": round(roof * 1e6, 3),
-                        "roofline_frac": round(roof / t, 4),
-                        "bound": "tensor" if sh.flops / (peaks["bf16_tflops"] * 1e12) >=
-                                 sh.compulsory_bytes / (peaks["hbm_gbs"] * 1e9) else "hbm",
-                        "kernel": plan["algo"], "tile": [plan["block_m"], plan["block_n"], plan["block_k"]],
-                        "grid": plan["grid"]}
-    dom = LAYERS[DOMINANT]
-    dom_t = per_layer_us[DOMINANT] * 1e-6
-    achieved = dom.flops / dom_t / 1e12
-    traffic = recorded_traffic(DOMINANT)
-    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": traffic, "kernel": f"{DOMINANT} layer forward ({per_layer[DOMINANT]['kernel']})",
-                "peak_source": f"{peak_src} bf16 dense (burst)",
-                "algorithmic_flops_per_launch": dom.flops}
+                        "roofline_us": round(max(t_flop, t_byte) * 1e6, 3),
+                        "roofline_frac": round(max(t_flop, t_byte) / t, 4),
+                        "bound": "tensor" if t_flop >= t_byte else "hbm",
+                        "kernel": pl["algo"], "tile": [pl["block_m"], pl["block_n"], pl["block_k"]],
+                        "grid": pl["grid"]}
+    dom = LAYERS[dominant]
+    dom_t = dom_us * 1e-6
+    if per_layer[dominant]["bound"] == "tensor":
+        achieved, peak, unit, bound = dom.flops / dom_t / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor"
+        per_launch = {"algorithmic_flops_per_launch": dom.flops}
+    else:
+        achieved, peak, unit, bound = dom.compulsory_bytes / dom_t / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
+        per_launch = {"algorithmic_bytes_per_launch": dom.compulsory_bytes}
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(dominant),
+                "kernel": f"{dominant} layer forward ({per_layer[dominant]['kernel']})",
+                "launch_us": round(dom_us, 3),
+                "peak_source": f"{peak_src} ({'bf16 dense burst' if bound == 'tensor' else 'HBM copy'})",
+                **per_launch}
 
-    e2e = run_e2e(args, capi, inputs, dev, stream, world)
+    e2e = run_e2e(args, capi, inputs, dev, stream, world) if args.e2e_steps > 0 else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.cpu_baseline_seconds)
+        cpu = cpu_baseline(args.cpu_baseline_seconds, layers)
 
     value = aggregate_throughput(flops_step * K, world, elapsed_max) / 1e12
+    workload = WORKLOAD if layers == LAYER_ORDER else \
+        "subset of the five-layer step: " + ", ".join(LAYERS[n].description for n in layers)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(elapsed_max / K * 1e3, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded PCG64: x~N(0,1), W~N(0,2/fan_in), BN gamma~U(.5,1.5), "
                 "beta,mean~N(0,.1), var~U(.5,2), eps=1e-3)",
-        "config": {"workload": WORKLOAD, "flops_per_step": flops_step,
-                   "l2": f"{ROTATION} rotating buffer sets (~426 MB per rotation > 129 MB L2)",
+        "config": {"workload": workload, "flops_per_step": flops_step,
+                   "l2": f"{ROTATION} rotating buffer sets (~426 MB per rotation > 129 MB L2); "
+                         "per_layer times: L2 flushed (512 MB write) before each call",
+                   "launch": ("direct API calls" if args.no_graphs else
+                              "CUDA graphs captured from the API calls, replayed per step"),
                    "parallelism": f"replicas x{world} (each rank runs the full step)"},
         "roofline": roofline,
         "per_layer": per_layer,
@@ -320,20 +417,45 @@ def run_ours(args, rank, world, local_rank):
     barrier(world)
 
 
+def isolated_layer_times(capi, sets, layers, stream, dev, iters) -> dict:
+    """Median forward time of each layer alone: the L2 is flushed (a 512 MB write) before
+    every call and CUDA events on the stream bracket the forward kernel only."""
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    out = {}
+    with torch.cuda.stream(stream):
+        for n in layers:
+            evs = []
+            for i in range(iters):
+                lb = sets[i % ROTATION][n]
+                sh = lb.shape
+                flush.zero_()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                capi.forward(lb.x, lb.w, lb.scale, lb.bias, sh.stride, sh.pad, y=lb.y, stream=stream)
+                b.record(stream)
+                evs.append((a, b))
+            torch.cuda.synchronize()
+            out[n] = 1e3 * statistics.median(a.elapsed_time(b) for a, b in evs)
+    del flush
+    return out
+
+
 def run_e2e(args, capi, inputs, dev, stream, world):
     """Same metric through the public API with host buffers: per step, every layer's x goes
     host->device from pinned memory, the fold and fused forward run, and y comes back
     device->host into pinned memory.  Weights and BN statistics stay resident on the device."""
-    host_x = {n: bits_to_torch_bf16(inputs[n].x_bits).pin_memory() for n in LAYER_ORDER}
-    bufs = {n: LayerBuffers(inputs[n], dev) for n in LAYER_ORDER}
-    host_y = {n: torch.empty(bufs[n].y.shape, dtype=torch.bfloat16).pin_memory() for n in LAYER_ORDER}
+    layers = args.layers
+    host_x = {n: bits_to_torch_bf16(inputs[n].x_bits).pin_memory() for n in layers}
+    bufs = {n: LayerBuffers(inputs[n], dev) for n in layers}
+    host_y = {n: torch.empty(bufs[n].y.shape, dtype=torch.bfloat16).pin_memory() for n in layers}
     h2d = sum(t.numel() * 2 for t in host_x.values())
     d2h = sum(t.numel() * 2 for t in host_y.values())
-    flops_step = sum(LAYERS[n].flops for n in LAYER_ORDER)
+    flops_step = sum(LAYERS[n].flops for n in layers)
 
     def step():
         with torch.cuda.stream(stream):
-            for n in LAYER_ORDER:
+            for n in layers:
                 b = bufs[n]
                 sh = b.shape
                 b.x.copy_(host_x[n], non_blocking=True)
@@ -366,7 +488,7 @@ def oracle_sample_step(pixels_per_layer: dict, inputs) -> int:
     """One oracle pass over a sample of output pixels of every layer; returns its flops."""
     import oracle
     flops = 0
-    for n in LAYER_ORDER:
+    for n in pixels_per_layer:
         inp = inputs[n]
         sh = inp.shape
         pix = pixels_per_layer[n]
@@ -379,27 +501,30 @@ def oracle_sample_step(pixels_per_layer: dict, inputs) -> int:
 def sample_pixels(fraction: float, inputs, seed: int = 0) -> dict:
     """The same fraction of every layer's output pixels (at least one), chosen evenly."""
     out = {}
-    for n in LAYER_ORDER:
+    for n in inputs:
         m = inputs[n].shape.m
         cnt = max(1, int(round(m * fraction)))
         out[n] = np.linspace(0, m - 1, cnt).astype(np.int64)
     return out
 
 
-def cpu_baseline(seconds: float) -> dict:
-    """The oracle as it stands, on this host's cores, over a bounded sample of the workload."""
+def cpu_baseline(seconds: float, layers=LAYER_ORDER) -> dict:
+    """The oracle as it stands, on this host's cores, over a bounded sample of the workload.
+
+    The sample is the same fraction of every layer's output pixels; the fraction grows
+    until one pass takes about `seconds` (each pass also decodes the layer's whole input,
+    so the time is not proportional to the fraction)."""
     import oracle
-    inputs = {n: make_layer_inputs(LAYERS[n]) for n in LAYER_ORDER}
+    inputs = {n: make_layer_inputs(LAYERS[n]) for n in layers}
     frac = 1e-4
-    t0 = time.perf_counter()
-    flops = oracle_sample_step(sample_pixels(frac, inputs), inputs)
-    dt = time.perf_counter() - t0
-    # scale the sample so the timed pass takes about `seconds`
-    frac = min(1.0, frac * max(1.0, seconds / max(dt, 1e-3)))
-    pix = sample_pixels(frac, inputs)
-    t0 = time.perf_counter()
-    flops = oracle_sample_step(pix, inputs)
-    dt = time.perf_counter() - t0
+    while True:
+        pix = sample_pixels(frac, inputs)
+        t0 = time.perf_counter()
+        flops = oracle_sample_step(pix, inputs)
+        dt = time.perf_counter() - t0
+        if dt >= seconds / 2 or frac >= 1.0:
+            break
+        frac = min(1.0, frac * max(2.0, min(8.0, seconds / max(dt, 1e-3) / 2)))
     return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": oracle.default_threads(),
             "kind": "oracle",
             "sample": f"{frac:.3g} of every layer's output pixels (evenly spaced, all channels), "
@@ -412,7 +537,7 @@ def run_reference(args, rank, world):
         return
     import oracle
     oracle.build()
-    inputs = {n: make_layer_inputs(LAYERS[n]) for n in LAYER_ORDER}
+    inputs = {n: make_layer_inputs(LAYERS[n]) for n in args.layers}
     total_steps = max(1, args.steps + args.warmup)
     target_step_s = max(1e-3, args.reference_budget_seconds / total_steps)
     frac = 1e-5

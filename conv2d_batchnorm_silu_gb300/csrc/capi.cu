@@ -6,7 +6,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/conv_bn_silu.h"
+#include "conv_bn_silu.h"
 #include "cbs_internal.h"
 
 namespace {

@@ -208,6 +208,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = dev::idesc_bf16_f32(C::BM, BN);
+            // Descriptors are built once; per stage and per K step only the start
+            // address field (16-byte units, low bits) advances.  The single issuing
+            // thread must spend almost nothing per MMA or it, not the tensor core,
+            // sets the pace.
+            const uint64_t desc_a0 = dev::smem_desc_kmajor(dev::smem_u32(sm_a), C::ROW_A);
+            const uint64_t desc_b0 = dev::smem_desc_kmajor(dev::smem_u32(sm_b), C::ROW_A);
             int stage = 0;
             uint32_t phase = 0;
             int lt = 0;
@@ -230,14 +236,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     dev::tc_fence_after_sync();
-                    const uint32_t a_addr = dev::smem_u32(sm_a + stage * C::A_STRIDE);
-                    const uint32_t b_addr = dev::smem_u32(sm_b + stage * C::B_STRIDE);
+                    const uint64_t da = desc_a0 + (uint64_t)(stage * (C::A_STRIDE >> 4));
+                    const uint64_t db = desc_b0 + (uint64_t)(stage * (C::B_STRIDE >> 4));
+                    dev::tc_mma_bf16(d_tmem, da, db, idesc, it != 0 ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t da = dev::smem_desc_kmajor(a_addr + kk * 32, C::ROW_A);
-                        const uint64_t db = dev::smem_desc_kmajor(b_addr + kk * 32, C::ROW_A);
-                        dev::tc_mma_bf16(d_tmem, da, db, idesc, (it | kk) != 0 ? 1u : 0u);
-                    }
+                    for (int kk = 1; kk < BK / 16; ++kk)
+                        dev::tc_mma_bf16(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, 1u);
                     dev::tc_commit(dev::smem_u32(&empty[stage]));
                     if (++stage == STAGES) {
                         stage = 0;

@@ -216,3 +216,27 @@ def test_streams_are_honoured(capi):
     side.synchronize()
     capi.check(side)
     assert_parity(y_to_f64(y), oracle_full(inp), "side stream")
+
+
+def test_silu_over_a_wide_range(capi):
+    """A 1x1 conv that copies one channel makes z sweep [-120, 120]: the epilogue's SiLU
+    must match the oracle over the whole range (saturation on both sides included)."""
+    from conv2d_batchnorm_silu_gb300.synthetic import f32_to_bf16_bits
+    shape = LayerShape("silu", 1, 64, 64, 16, 16, 1, 1, 1, 0)
+    inp = make_layer_inputs(shape, seed=9)
+    x = np.zeros((1, 64, 64, 16), np.float32)
+    x[..., 0] = np.linspace(-120.0, 120.0, 64 * 64, dtype=np.float32).reshape(64, 64)
+    x[..., 1] = np.linspace(-6.0, 6.0, 64 * 64, dtype=np.float32).reshape(64, 64)
+    w = np.zeros((16, 1, 1, 16), np.float32)
+    w[:8, 0, 0, 0] = 1.0
+    w[8:, 0, 0, 1] = 1.0
+    inp.x_bits = f32_to_bf16_bits(x)
+    inp.w_bits = f32_to_bf16_bits(w)
+    inp.gamma[:] = 1.0
+    inp.beta[:] = 0.0
+    inp.mean[:] = 0.0
+    inp.var[:] = 1.0
+    inp.eps = 0.0
+    for algo in ("auto", "direct"):
+        y = y_to_f64(run_gpu(capi, inp, algo=algo))
+        assert_parity(y, oracle_full(inp), f"SiLU sweep ({algo})")
