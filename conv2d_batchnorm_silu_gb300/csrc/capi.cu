@@ -182,6 +182,8 @@ int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, in
         out.threads = cbs::kTcThreads;
         out.smem_bytes = t.smem_bytes;
         out.k_iters = t.k_iters;
+        out.stream_k = t.stream_k;
+        out.workspace_bytes = t.workspace_bytes;
     } else {
         const long long bx = (p.m + cbs::kDirectThreads - 1) / cbs::kDirectThreads;
         const int by = (c_out + cbs::kDirectBlockN - 1) / cbs::kDirectBlockN;
@@ -204,7 +206,11 @@ int conv_bn_silu_check(void *stream)
     unsigned int word = 0;
     cudaError_t e = cbs::tc_read_and_clear_error(static_cast<cudaStream_t>(stream), &word);
     if (e != cudaSuccess) return cuda_fail(e);
-    return word != 0 ? CBS_ERR_TIMEOUT : CBS_OK;
+    if (word == 0) return CBS_OK;
+    // A kernel gave up mid-way: stream-K ready flags may be left raised.
+    e = cbs::tc_reset_workspaces();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CBS_ERR_TIMEOUT;
 }
 
 const char *conv_bn_silu_status_string(int status)

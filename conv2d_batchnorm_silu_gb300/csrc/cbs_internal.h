@@ -30,6 +30,9 @@ struct TcPlan {
     int m_tiles, n_tiles, tiles;
     int grid;
     int smem_bytes;
+    int stream_k;                 // 1: K steps split evenly over the grid (see tc_conv.cu)
+    long long workspace_bytes;    // stream-K partial tiles + flags (0 when not split)
+    long long flag_bytes;         // the leading part of the workspace that must start zeroed
 };
 
 constexpr int kTcBlockM = 128;
@@ -50,6 +53,9 @@ cudaError_t fold_launch(const float *gamma, const float *beta, const float *mean
 
 // Device error words (one per kernel translation unit): read and clear, stream-ordered.
 cudaError_t tc_read_and_clear_error(cudaStream_t stream, unsigned int *out);
+// Re-zeroes the stream-K ready flags of every workspace the library holds (after a
+// kernel gave up mid-way, flags may be left raised).  Synchronous.
+cudaError_t tc_reset_workspaces();
 
 // Device error codes written by kernels (bit flags).
 constexpr unsigned int kErrTimeoutProducer = 1u;

@@ -51,7 +51,80 @@ struct TcArgs {
     int stride_h, stride_w, pad_h, pad_w;
     int s;
     int c_chunks, k_iters;
+    int stream_k;    // 1: each CTA takes an equal share of all K steps (see WorkIter)
+    float *partial;  // stream-K: [grid-1][128*BN] fp32 partial tiles (slot c: boundary of CTAs c, c+1)
+    int *flags;      // stream-K: [grid-1][4] ready flags, one per epilogue warp; 0 between launches
 };
+
+// K steps [kb, ke) of output tile `tile`.
+struct WorkUnit {
+    int tile, kb, ke;
+};
+
+// The units one CTA processes, in order.  Data-parallel: whole tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ...  Stream-K: the CTA's equal share [g, g_end) of the
+// global K-step sequence (tile-major), cut at tile boundaries.  The host enables
+// stream-K only when every share is at least one tile long, so a unit is a whole
+// tile, the tail of a tile (kb > 0: the previous CTA holds its head) or the head
+// of a tile (ke < k_iters: the next CTA holds its tail), never a middle piece.
+struct WorkIter {
+    long long g, g_end;
+    int t;
+    __device__ explicit WorkIter(const TcArgs &a)
+    {
+        const long long total = (long long)a.tiles * a.k_iters;
+        g = a.stream_k ? total * blockIdx.x / gridDim.x : 0;
+        g_end = a.stream_k ? total * (blockIdx.x + 1) / gridDim.x : 0;
+        t = blockIdx.x;
+    }
+    __device__ bool next(const TcArgs &a, WorkUnit &u)
+    {
+        if (a.stream_k) {
+            if (g >= g_end) return false;
+            u.tile = (int)(g / a.k_iters);
+            u.kb = (int)(g - (long long)u.tile * a.k_iters);
+            const long long left = g_end - g;
+            u.ke = left < (long long)(a.k_iters - u.kb) ? u.kb + (int)left : a.k_iters;
+            g += u.ke - u.kb;
+            return true;
+        }
+        if (t >= a.tiles) return false;
+        u.tile = t;
+        u.kb = 0;
+        u.ke = a.k_iters;
+        t += gridDim.x;
+        return true;
+    }
+};
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int *p, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait for another CTA's flag (both CTAs are resident: the grid never
+// exceeds one CTA per SM).  False on timeout or when this CTA is aborting.
+__device__ __forceinline__ bool wait_flag_bounded(const int *flag, const volatile int *abort_flag,
+                                                  uint64_t timeout_ns)
+{
+    if (ld_acquire_gpu(flag) != 0) return true;
+    const uint64_t t0 = dev::globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ld_acquire_gpu(flag) != 0) return true;
+        if ((i & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (dev::globaltimer_ns() - t0 > timeout_ns) return false;
+        }
+        __nanosleep(64);
+    }
+}
 
 template <int BN, int BK>
 struct TcCfg {
@@ -152,9 +225,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issued_parity = 0;
-            for (int t = blockIdx.x; t < a.tiles && !*abort_flag; t += gridDim.x) {
-                const int m_tile = t / a.n_tiles;
-                const int n0 = (t - m_tile * a.n_tiles) * BN;
+            WorkIter wi(a);
+            WorkUnit u;
+            while (!*abort_flag && wi.next(a, u)) {
+                const int m_tile = u.tile / a.n_tiles;
+                const int n0 = (u.tile - m_tile * a.n_tiles) * BN;
                 const int m0 = m_tile * C::BM;
                 const int img = m0 / a.howo;
                 const int rem = m0 - img * a.howo;
@@ -162,9 +237,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int ow = rem - oh * a.wo;
                 const int corner_w = ow * a.stride_w - a.pad_w;
                 const int corner_h = oh * a.stride_h - a.pad_h;
-                int r = 0, s = 0, cc = 0;
+                int cc = u.kb % a.c_chunks;
+                int s = (u.kb / a.c_chunks) % a.s;
+                int r = (u.kb / a.c_chunks) / a.s;
                 bool ok = true;
-                for (int it = 0; it < a.k_iters; ++it) {
+                for (int it = u.kb; it < u.ke; ++it) {
                     const uint32_t e_bar = dev::smem_u32(&empty[stage]);
                     if (!dev::mbar_wait_bounded(e_bar, phase ^ 1u, abort_flag, kWaitTimeoutNs)) {
                         if (!*abort_flag) record_error(kErrTimeoutProducer, abort_flag);
@@ -218,7 +295,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t phase = 0;
             int lt = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < a.tiles && ok; t += gridDim.x, ++lt) {
+            WorkIter wi(a);
+            WorkUnit u;
+            for (; ok && wi.next(a, u); ++lt) {
                 const int buf = lt & 1;
                 const uint32_t tparity = (uint32_t)(lt >> 1) & 1u;
                 if (!dev::mbar_wait_bounded(dev::smem_u32(&tempty[buf]), tparity ^ 1u, abort_flag,
@@ -228,7 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 dev::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-                for (int it = 0; it < a.k_iters; ++it) {
+                for (int it = u.kb; it < u.ke; ++it) {
                     if (!dev::mbar_wait_bounded(dev::smem_u32(&full[stage]), phase, abort_flag,
                                                 kWaitTimeoutNs)) {
                         if (!*abort_flag) record_error(kErrTimeoutMma, abort_flag);
@@ -238,7 +317,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     dev::tc_fence_after_sync();
                     const uint64_t da = desc_a0 + (uint64_t)(stage * (C::A_STRIDE >> 4));
                     const uint64_t db = desc_b0 + (uint64_t)(stage * (C::B_STRIDE >> 4));
-                    dev::tc_mma_bf16(d_tmem, da, db, idesc, it != 0 ? 1u : 0u);
+                    dev::tc_mma_bf16(d_tmem, da, db, idesc, it != u.kb ? 1u : 0u);
 #pragma unroll
                     for (int kk = 1; kk < BK / 16; ++kk)
                         dev::tc_mma_bf16(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, 1u);
@@ -265,7 +344,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint8_t *my_stg = sm_stg + ew * 2 * C::STG_BYTES;
         int sbuf = 0;
         int lt = 0;
-        for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++lt) {
+        const int row = ew * 32 + lane;  // this thread's row of the tile (TMEM lane)
+        WorkIter wi(a);
+        WorkUnit u;
+        for (; wi.next(a, u); ++lt) {
             const int buf = lt & 1;
             const uint32_t tparity = (uint32_t)(lt >> 1) & 1u;
             int ok = 1;
@@ -280,9 +362,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             dev::tc_fence_after_sync();
-            const int m_tile = t / a.n_tiles;
-            const int n0 = (t - m_tile * a.n_tiles) * BN;
+            const int m_tile = u.tile / a.n_tiles;
+            const int n0 = (u.tile - m_tile * a.n_tiles) * BN;
             const int row0 = m_tile * C::BM + ew * 32;  // first output pixel of this warp
+            // Stream-K: the tail of a split tile leaves its fp32 partial sums for the
+            // CTA holding the head, which adds them (in a fixed order) and finishes.
+            const bool publish = u.kb > 0;
+            const bool combine = u.ke < a.k_iters;
+            const int slot = publish ? (int)blockIdx.x - 1 : (int)blockIdx.x;
+            float4 *part = a.stream_k ? reinterpret_cast<float4 *>(a.partial) + (size_t)slot * (32 * BN)
+                                      : nullptr;
+            if (combine) {
+                int got = 1;
+                if (lane == 0) got = wait_flag_bounded(a.flags + slot * 4 + ew, abort_flag, kWaitTimeoutNs) ? 1 : 0;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    if (lane == 0 && !*abort_flag) record_error(kErrTimeoutEpilogue, abort_flag);
+                    break;
+                }
+                __threadfence();
+            }
             const uint32_t t_lane = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN);
 #pragma unroll 1
             for (int j = 0; j < BN / EC; ++j) {
@@ -298,6 +397,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     dev::tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
+                }
+                if (publish) {
+                    // Column-group-major, row-minor: a warp writes 512 contiguous bytes per store.
+#pragma unroll
+                    for (int q = 0; q < EC / 4; ++q)
+                        __stcg(part + (size_t)(j * (EC / 4) + q) * C::BM + row,
+                               make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+                    continue;
+                }
+                if (combine) {
+#pragma unroll
+                    for (int q = 0; q < EC / 4; ++q) {
+                        const float4 p4 = __ldcg(part + (size_t)(j * (EC / 4) + q) * C::BM + row);
+                        v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) + p4.x);
+                        v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + p4.y);
+                        v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + p4.z);
+                        v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + p4.w);
+                    }
                 }
                 const int ch0 = n0 + j * EC;
                 uint32_t packed[EC / 2];
@@ -341,6 +459,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     dev::bulk_commit_group();
                 }
                 sbuf ^= 1;
+            }
+            if (publish) {
+                // Every lane's partial sums are visible GPU-wide before the flag rises.
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(a.flags + slot * 4 + ew, 1);
+            } else if (combine) {
+                __syncwarp();  // all lanes have read the partial: the slot is free again
+                if (lane == 0) st_release_gpu(a.flags + slot * 4 + ew, 0);
             }
         }
         if (lane == 0) dev::bulk_wait_group<0>();
@@ -503,6 +630,58 @@ cudaError_t cached_maps(const ConvProblem &p, int block_n, int block_k, TcMaps *
     return cudaSuccess;
 }
 
+// Stream-K scratch, one buffer per (device, stream) so that calls on different
+// streams never share it; grown on demand with cudaMalloc, ready flags zeroed
+// when (re)allocated.  Kernels leave every flag at zero when they finish.
+struct Workspace {
+    int device;
+    cudaStream_t stream;
+    void *ptr;
+    size_t bytes, flag_bytes;
+};
+std::mutex g_ws_mu;
+Workspace g_ws[64];
+int g_ws_count = 0;
+
+cudaError_t stream_k_workspace(cudaStream_t stream, size_t bytes, size_t flag_bytes, void **out)
+{
+    int device = 0;
+    cudaError_t st = cudaGetDevice(&device);
+    if (st != cudaSuccess) return st;
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    Workspace *w = nullptr;
+    for (int i = 0; i < g_ws_count; ++i)
+        if (g_ws[i].device == device && g_ws[i].stream == stream) w = &g_ws[i];
+    if (w && w->bytes >= bytes && w->flag_bytes >= flag_bytes) {
+        *out = w->ptr;
+        return cudaSuccess;
+    }
+    if (!w) {
+        if (g_ws_count == 64) return cudaErrorMemoryAllocation;
+        w = &g_ws[g_ws_count++];
+        *w = Workspace{device, stream, nullptr, 0, 0};
+    } else if (w->ptr) {
+        st = cudaStreamSynchronize(stream);  // the old buffer may still be in use
+        if (st != cudaSuccess) return st;
+        cudaFree(w->ptr);
+        w->ptr = nullptr;
+        w->bytes = w->flag_bytes = 0;
+    }
+    void *ptr = nullptr;
+    st = cudaMalloc(&ptr, bytes);
+    if (st != cudaSuccess) return st;
+    st = cudaMemsetAsync(ptr, 0, flag_bytes, stream);
+    if (st != cudaSuccess) {
+        cudaFree(ptr);
+        return st;
+    }
+    w->ptr = ptr;
+    w->bytes = bytes;
+    w->flag_bytes = flag_bytes;
+    *out = ptr;
+    return cudaSuccess;
+}
+
 template <int BN, int BK>
 cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &maps, cudaStream_t stream)
 {
@@ -539,6 +718,16 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
     a.s = p.s;
     a.c_chunks = plan.c_chunks;
     a.k_iters = plan.k_iters;
+    a.stream_k = plan.stream_k;
+    a.partial = nullptr;
+    a.flags = nullptr;
+    if (plan.stream_k) {
+        void *ws = nullptr;
+        st = stream_k_workspace(stream, (size_t)plan.workspace_bytes, (size_t)plan.flag_bytes, &ws);
+        if (st != cudaSuccess) return st;
+        a.flags = static_cast<int *>(ws);
+        a.partial = reinterpret_cast<float *>(static_cast<char *>(ws) + plan.flag_bytes);
+    }
     kern<<<plan.grid, kTcThreads, C::SMEM, stream>>>(maps.x, maps.w, maps.y, a);
     return cudaGetLastError();
 }
@@ -581,9 +770,16 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
 {
     TcPlan t{};
     t.block_k = p.c % 64 == 0 ? 64 : (p.c % 32 == 0 ? 32 : 16);
+    t.c_chunks = (p.c + t.block_k - 1) / t.block_k;
+    t.k_iters = p.r * p.s * t.c_chunks;
     const int m_tiles = (int)((p.m + kTcBlockM - 1) / kTcBlockM);
+    const long long tiles256 = (long long)m_tiles * ((p.c_out + 255) / 256);
     if (p.c_out <= 128) {
         t.block_n = p.c_out <= 16 ? 16 : (p.c_out <= 32 ? 32 : (p.c_out <= 64 ? 64 : 128));
+    } else if (t.k_iters >= 16 && tiles256 >= sm_count) {
+        // Long K loops are tensor-bound: the widest tile (N = 256) moves the fewest
+        // shared-memory bytes per MMA, and stream-K (below) evens out the waves.
+        t.block_n = 256;
     } else {
         // Choose 128 or 256 output channels per tile by the estimated number of
         // waves times the per-tile work (which scales with the tile width).
@@ -599,13 +795,26 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
         }
     }
     t.stages = stages_for(t.block_n, t.block_k);
-    t.c_chunks = (p.c + t.block_k - 1) / t.block_k;
-    t.k_iters = p.r * p.s * t.c_chunks;
     t.m_tiles = m_tiles;
     t.n_tiles = (p.c_out + t.block_n - 1) / t.block_n;
     t.tiles = t.m_tiles * t.n_tiles;
     t.grid = std::min(t.tiles, sm_count);
     t.smem_bytes = tc_smem_bytes(t.block_n, t.block_k, t.stages);
+    // Stream-K when whole tiles would leave a partly idle last wave: every CTA
+    // takes total/grid consecutive K steps.  Each share must cover at least one
+    // tile so that a tile is split between two CTAs at most.
+    const long long total = (long long)t.tiles * t.k_iters;
+    t.stream_k = (t.tiles > sm_count && t.tiles % sm_count != 0 && t.tiles < 4LL * sm_count &&
+                  t.k_iters >= 16 && total / sm_count >= t.k_iters)
+                     ? 1
+                     : 0;
+    t.workspace_bytes = 0;
+    t.flag_bytes = 0;
+    if (t.stream_k) {
+        t.grid = sm_count;
+        t.flag_bytes = ((long long)(t.grid - 1) * 4 * (long long)sizeof(int) + 255) / 256 * 256;
+        t.workspace_bytes = t.flag_bytes + (long long)(t.grid - 1) * kTcBlockM * t.block_n * 4;
+    }
     return t;
 }
 
@@ -623,6 +832,22 @@ cudaError_t tc_launch(const ConvProblem &p, const TcPlan &plan, cudaStream_t str
     CBS_TC_CASE(256, 16) CBS_TC_CASE(256, 32) CBS_TC_CASE(256, 64)
 #undef CBS_TC_CASE
     return cudaErrorInvalidConfiguration;
+}
+
+cudaError_t tc_reset_workspaces()
+{
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    int prev = 0;
+    cudaError_t st = cudaGetDevice(&prev);
+    if (st != cudaSuccess) return st;
+    for (int i = 0; i < g_ws_count && st == cudaSuccess; ++i) {
+        if (!g_ws[i].ptr) continue;
+        st = cudaSetDevice(g_ws[i].device);
+        if (st == cudaSuccess) st = cudaStreamSynchronize(g_ws[i].stream);
+        if (st == cudaSuccess) st = cudaMemset(g_ws[i].ptr, 0, g_ws[i].flag_bytes);
+    }
+    cudaSetDevice(prev);
+    return st;
 }
 
 cudaError_t tc_read_and_clear_error(cudaStream_t stream, unsigned int *out)

@@ -113,6 +113,8 @@ typedef struct cbs_plan_info {
     int threads;      /* threads per CTA */
     int smem_bytes;   /* dynamic shared memory per CTA */
     int k_iters;      /* pipeline steps per tile */
+    int stream_k;     /* 1 when the K steps of all tiles are split evenly over the grid */
+    long long workspace_bytes; /* library-held scratch for stream-K partial tiles (0 if none) */
 } cbs_plan_info;
 
 /* Fills `info` for the given shape, algorithm and SM count (sm_count > 0;

@@ -70,6 +70,10 @@ def test_plan_for_the_five_layers(lib):
         if p["algo"] == "tcgen05":
             assert p["block_m"] == 128 and p["block_n"] % 16 == 0 and p["block_n"] <= 256
             assert p["block_n"] >= min(sh.k, 128)
+            assert p["stream_k"] == (1 if name == "deep" else 0)
+            if p["stream_k"]:
+                assert p["block_n"] == 256 and p["grid"] == 152
+                assert p["workspace_bytes"] >= 151 * 128 * 256 * 4
             assert p["grid"] <= 152 and p["grid"] <= p["tiles"]
             assert p["smem_bytes"] <= 232448
             assert p["stages"] >= 2

@@ -240,3 +240,26 @@ def test_silu_over_a_wide_range(capi):
     for algo in ("auto", "direct"):
         y = y_to_f64(run_gpu(capi, inp, algo=algo))
         assert_parity(y, oracle_full(inp), f"SiLU sweep ({algo})")
+
+
+STREAM_K_CASES = [
+    # n, h, w, c, k, r, s, stride, pad: more 128x256 tiles than SMs, K loop >= 16 steps
+    (32, 20, 20, 128, 512, 3, 3, 1, 1),   # 200 tiles, 18 K steps
+    (39, 20, 20, 256, 384, 3, 3, 1, 1),   # 244 tiles, ragged last M tile, a 128-channel N tail
+]
+
+
+@pytest.mark.parametrize("case", STREAM_K_CASES, ids=["200tiles", "244tiles_ragged"])
+def test_stream_k_split_tiles(capi, case):
+    """Shapes whose plan splits the K loop of some tiles between two CTAs (stream-K):
+    every output matches the oracle and two runs are bit-identical (the partial sums
+    are combined in a fixed order and the ready flags return to zero)."""
+    n, h, w, c, k, r, s, stride, pad = case
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = capi.plan(n, h, w, c, k, r, s, stride, pad, "auto", sms)
+    assert p["algo"] == "tcgen05" and p["stream_k"] == 1 and p["block_n"] == 256, p
+    inp = make_layer_inputs(LayerShape("streamk", n, h, w, c, k, r, s, stride, pad), seed=31)
+    y1 = run_gpu(capi, inp)
+    y2 = run_gpu(capi, inp)
+    assert np.array_equal(torch_bf16_to_bits(y1), torch_bf16_to_bits(y2))
+    assert_parity(y_to_f64(y1), oracle_full(inp), f"{case} (stream-K)")
