@@ -59,6 +59,7 @@ def _declare(name, argtypes, restype=ctypes.c_int):
 _fold = _declare("conv_bn_silu_fold", [_p, _p, _p, _p, _f, _i, _p, _p, _p])
 _forward = _declare("conv_bn_silu_forward", [_p] * 5 + [_i] * 11 + [_p])
 _forward_algo = _declare("conv_bn_silu_forward_algo", [_p] * 5 + [_i] * 12 + [_p])
+_forward_noalloc = _declare("conv_bn_silu_forward_noalloc", [_p] * 5 + [_i] * 11 + [_p])
 _output_dims = _declare("conv_bn_silu_output_dims", [_i] * 8 + [ctypes.POINTER(_i)] * 2)
 _plan = _declare("conv_bn_silu_plan", [_i] * 13 + [ctypes.POINTER(PlanInfo)])
 _check = _declare("conv_bn_silu_check", [_p])
@@ -179,6 +180,36 @@ def forward(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor, bias: torch.T
     st = _forward_algo(px, pw_, ps, pb, py, n, h, wi, c, c_out, r, s, sh, sw, ph, pw,
                        ALGOS[algo], _stream_handle(stream))
     _raise_if(st, "conv_bn_silu_forward")
+    return y
+
+
+def forward_noalloc(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor, bias: torch.Tensor,
+                    y: torch.Tensor, stride=1, pad=0, stream=None) -> torch.Tensor:
+    """conv_bn_silu_forward_noalloc: the fused forward without any device allocation.
+
+    For callers that must not allocate (fixed memory budgets, allocator-owned
+    memory, capture-sensitive loops): the caller supplies y, and the library uses
+    a fixed 20 MiB device array for its stream-K scratch.  Calls that overlap on
+    the GPU share that array and race; serialise them on one stream.
+    """
+    if x.dim() != 4 or w.dim() != 4:
+        raise ValueError("x must be NHWC and w KRSC (4-D)")
+    n, h, wi, c = x.shape
+    c_out, r, s, c2 = w.shape
+    if c2 != c:
+        raise ValueError(f"channel mismatch: x has {c}, w has {c2}")
+    sh, sw = _pair(stride)
+    ph, pw = _pair(pad)
+    ho, wo = output_dims(h, wi, r, s, (sh, sw), (ph, pw))
+    if tuple(y.shape) != (n, ho, wo, c_out):
+        raise ValueError(f"y has shape {tuple(y.shape)}, expected {(n, ho, wo, c_out)}")
+    if y.numel() == 0:
+        return y
+    st = _forward_noalloc(_dev_tensor(x, torch.bfloat16, "x"), _dev_tensor(w, torch.bfloat16, "w"),
+                          _dev_tensor(scale, torch.float32, "scale"),
+                          _dev_tensor(bias, torch.float32, "bias"), _dev_tensor(y, torch.bfloat16, "y"),
+                          n, h, wi, c, c_out, r, s, sh, sw, ph, pw, _stream_handle(stream))
+    _raise_if(st, "conv_bn_silu_forward_noalloc")
     return y
 
 

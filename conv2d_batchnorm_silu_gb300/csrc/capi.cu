@@ -94,9 +94,77 @@ int sm_count_current_device(int *count)
     return CBS_OK;
 }
 
+// ------------------------------------------------------------------ allocation-free forward
+// Scratch for conv_bn_silu_forward_noalloc: the stream-K partial tiles and ready
+// flags live in this fixed device array instead of library-allocated memory.
+// It is zero-initialised when the module loads; every GPU that loads the
+// library holds it until the process exits.  In host code the symbol is only a
+// stand-in: its device address comes from cudaGetSymbolAddress below.
+constexpr size_t kNoAllocScratchBytes = 20u << 20;  // 20 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device (on that device's first call) and cached.
+int noalloc_scratch_address(void **out)
+{
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= 64) return CBS_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return CBS_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int conv_bn_silu_forward_noalloc(const void *x, const void *w, const float *scale, const float *bias,
+                                 void *y, int n, int h, int w_in, int c, int c_out, int r, int s,
+                                 int stride_h, int stride_w, int pad_h, int pad_w, void *stream)
+{
+    cbs::ConvProblem p{};
+    int st = make_problem(n, h, w_in, c, c_out, r, s, stride_h, stride_w, pad_h, pad_w, &p);
+    if (st != CBS_OK) return st;
+    if (p.m == 0 || c_out == 0) return CBS_OK;
+    if (!x || !w || !scale || !bias || !y) return CBS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(scale) || !aligned16(bias) || !aligned16(y))
+        return CBS_ERR_MISALIGNED;
+    p.x = x;
+    p.w = w;
+    p.scale = scale;
+    p.bias = bias;
+    p.y = y;
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    if (!cbs::tc_supported(p)) {
+        cudaError_t e = cbs::direct_launch(p, strm);  // needs no scratch
+        return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+    }
+    int sms = 0;
+    st = sm_count_current_device(&sms);
+    if (st != CBS_OK) return st;
+    const cbs::TcPlan plan = cbs::tc_make_plan(p, sms);
+    void *scratch = nullptr;
+    if (plan.stream_k) {
+        if (plan.workspace_bytes > (long long)kNoAllocScratchBytes) return CBS_ERR_UNSUPPORTED;
+        st = noalloc_scratch_address(&scratch);
+        if (st != CBS_OK) return st;
+        // The ready flags must start at zero; a previous call that gave up may have left some set.
+        cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)plan.flag_bytes, strm);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    cudaError_t e = cbs::tc_launch_with_workspace(p, plan, strm, scratch);
+    return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+}
 
 int conv_bn_silu_fold(const float *gamma, const float *beta, const float *mean, const float *var,
                       float eps, int c_out, float *scale, float *bias, void *stream)

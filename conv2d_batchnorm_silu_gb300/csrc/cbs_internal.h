@@ -47,6 +47,11 @@ int tc_smem_bytes(int block_n, int block_k, int stages);
 
 // Launchers; return cudaSuccess or the first CUDA error met.
 cudaError_t tc_launch(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream);
+// As tc_launch, but a stream-K plan uses `workspace` (plan.workspace_bytes long,
+// its first plan.flag_bytes zeroed) instead of the library-held buffer; nullptr
+// means the library-held buffer.
+cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream,
+                                     void *workspace);
 cudaError_t direct_launch(const ConvProblem &p, cudaStream_t stream);
 cudaError_t fold_launch(const float *gamma, const float *beta, const float *mean, const float *var,
                         float eps, int c_out, float *scale, float *bias, cudaStream_t stream);

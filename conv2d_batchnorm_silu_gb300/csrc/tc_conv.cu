@@ -683,7 +683,8 @@ cudaError_t stream_k_workspace(cudaStream_t stream, size_t bytes, size_t flag_by
 }
 
 template <int BN, int BK>
-cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &maps, cudaStream_t stream)
+cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &maps, cudaStream_t stream,
+                       void *caller_workspace)
 {
     using C = TcCfg<BN, BK>;
     auto kern = tc_conv_bn_silu_kernel<BN, BK>;
@@ -722,9 +723,11 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
     a.partial = nullptr;
     a.flags = nullptr;
     if (plan.stream_k) {
-        void *ws = nullptr;
-        st = stream_k_workspace(stream, (size_t)plan.workspace_bytes, (size_t)plan.flag_bytes, &ws);
-        if (st != cudaSuccess) return st;
+        void *ws = caller_workspace;
+        if (ws == nullptr) {
+            st = stream_k_workspace(stream, (size_t)plan.workspace_bytes, (size_t)plan.flag_bytes, &ws);
+            if (st != cudaSuccess) return st;
+        }
         a.flags = static_cast<int *>(ws);
         a.partial = reinterpret_cast<float *>(static_cast<char *>(ws) + plan.flag_bytes);
     }
@@ -820,11 +823,18 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
 
 cudaError_t tc_launch(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream)
 {
+    return tc_launch_with_workspace(p, plan, stream, nullptr);
+}
+
+cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream,
+                                     void *workspace)
+{
     TcMaps maps;
     cudaError_t st = cached_maps(p, plan.block_n, plan.block_k, &maps);
     if (st != cudaSuccess) return st;
 #define CBS_TC_CASE(BN_, BK_) \
-    if (plan.block_n == BN_ && plan.block_k == BK_) return launch_cfg<BN_, BK_>(p, plan, maps, stream);
+    if (plan.block_n == BN_ && plan.block_k == BK_)       \
+        return launch_cfg<BN_, BK_>(p, plan, maps, stream, workspace);
     CBS_TC_CASE(16, 16) CBS_TC_CASE(16, 32) CBS_TC_CASE(16, 64)
     CBS_TC_CASE(32, 16) CBS_TC_CASE(32, 32) CBS_TC_CASE(32, 64)
     CBS_TC_CASE(64, 16) CBS_TC_CASE(64, 32) CBS_TC_CASE(64, 64)

@@ -95,6 +95,30 @@ int conv_bn_silu_forward_algo(const void *x, const void *w, const float *scale, 
                               int stride_h, int stride_w, int pad_h, int pad_w, int algo,
                               void *stream);
 
+/*
+ * Allocation-free variant of conv_bn_silu_forward (CBS_ALGO_AUTO), for callers
+ * that may not allocate device memory: code running under a framework's own
+ * caching allocator or a fixed memory budget, real-time loops where
+ * cudaMalloc's implicit synchronisation is not acceptable, or hosts that hand
+ * out only pre-sized buffers.  The fusion page has no counterpart to this; it
+ * is a deployment convenience of this library.
+ * Same arguments, layouts, results and errors as conv_bn_silu_forward.  Where
+ * the plan splits K loops between CTAs (stream-K), the partial tiles go to a
+ * fixed 20 MiB device array inside the library instead of a library-allocated
+ * buffer: shapes whose split needs more (see cbs_plan_info.workspace_bytes)
+ * return CBS_ERR_UNSUPPORTED.  Nothing is allocated by any call.
+ *   - The first call on a device looks up that array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array per device and clears its ready flags
+ *     first (an asynchronous memset on `stream`): calls whose kernels overlap
+ *     on the GPU, e.g. on two streams, race and may produce wrong results.
+ *     Serialise them on one stream.
+ */
+int conv_bn_silu_forward_noalloc(const void *x, const void *w, const float *scale, const float *bias,
+                                 void *y, int n, int h, int w_in, int c, int c_out, int r, int s,
+                                 int stride_h, int stride_w, int pad_h, int pad_w, void *stream);
+
 /* Output spatial size of the convolution; host only, touches no GPU.
  * ho = (h + 2*pad_h - r)/stride_h + 1, wo likewise; CBS_ERR_INVALID_ARG when
  * either would be < 1 or an argument is out of range. */
