@@ -66,8 +66,8 @@ int make_problem(int n, int h, int w_in, int c, int c_out, int r, int s, int sh,
 
 int select_algo(const cbs::ConvProblem &p, int algo)
 {
-    if (algo == CBS_ALGO_AUTO) return cbs::tc_supported(p) ? CBS_ALGO_TCGEN05 : CBS_ALGO_DIRECT;
-    return algo;
+    if (algo != CBS_ALGO_AUTO) return algo;
+    return cbs::tc_supported(p) ? CBS_ALGO_TCGEN05 : CBS_ALGO_DIRECT;
 }
 
 int sm_count_current_device(int *count)

@@ -36,7 +36,18 @@ struct TcPlan {
 };
 
 constexpr int kTcBlockM = 128;
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 384;  // producer, MMA, two idle, eight epilogue warps
+constexpr int kTcFlagsPerSlot = 8;  // stream-K ready flags: one per epilogue warp
+
+// Epilogue geometry of the tensor-core kernel for an N tile of `block_n`
+// channels: `split` warps share each 32-row TMEM lane quarter (each takes
+// block_n/split columns), processed `ec` columns at a time.
+inline void tc_epilogue_geometry(int block_n, int *split, int *ec)
+{
+    *split = block_n >= 64 ? 2 : 1;
+    const int cols = block_n / *split;
+    *ec = cols < 32 ? cols : 32;
+}
 constexpr int kDirectThreads = 128;
 constexpr int kDirectBlockN = 16;
 
@@ -53,6 +64,8 @@ cudaError_t tc_launch(const ConvProblem &p, const TcPlan &plan, cudaStream_t str
 cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream,
                                      void *workspace);
 cudaError_t direct_launch(const ConvProblem &p, cudaStream_t stream);
+// True when direct_launch has a fully unrolled variant for this filter shape.
+bool direct_small_available(int r, int s, int c);
 cudaError_t fold_launch(const float *gamma, const float *beta, const float *mean, const float *var,
                         float eps, int c_out, float *scale, float *bias, cudaStream_t stream);
 

@@ -16,9 +16,10 @@
 //   warp 1      MMA issuer: tcgen05.mma (M=128, N=BN, K=16) into a TMEM
 //               accumulator; two accumulators so the epilogue of tile i
 //               overlaps the K loop of tile i+1.
-//   warps 4..7  epilogue ("The shape of it"): tcgen05.ld of the finished tile,
-//               acc*scale + bias, SiLU, bf16 cast, staged through swizzled
-//               shared memory and written by TMA stores.  x is read once and y
+//   warps 4..11 epilogue ("The shape of it"): tcgen05.ld of the finished tile
+//               (warps w and w+4 share TMEM lanes 32*(w%4).. and split the
+//               columns), acc*scale + bias, SiLU, bf16 cast, staged through
+//               swizzled shared memory and written by TMA stores.  x is read once and y
 //               written once; the conv result never goes to memory.
 // Every mbarrier wait is bounded in time; on timeout the kernel records an
 // error bit, waits for its own copies in flight, frees TMEM and returns.
@@ -53,7 +54,7 @@ struct TcArgs {
     int c_chunks, k_iters;
     int stream_k;    // 1: each CTA takes an equal share of all K steps (see WorkIter)
     float *partial;  // stream-K: [grid-1][128*BN] fp32 partial tiles (slot c: boundary of CTAs c, c+1)
-    int *flags;      // stream-K: [grid-1][4] ready flags, one per epilogue warp; 0 between launches
+    int *flags;      // stream-K: [grid-1][8] ready flags, one per epilogue warp; 0 between launches
 };
 
 // K steps [kb, ke) of output tile `tile`.
@@ -133,9 +134,12 @@ struct TcCfg {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int A_STRIDE = (A_BYTES + 1023) / 1024 * 1024;
     static constexpr int B_STRIDE = (B_BYTES + 1023) / 1024 * 1024;
-    static constexpr int EC = BN < 64 ? BN : 64;  // epilogue columns per chunk
+    static constexpr int SPLIT = BN >= 64 ? 2 : 1;  // epilogue warps per TMEM lane quarter
+    static constexpr int EPI_COLS = BN / SPLIT;     // columns of the tile one epilogue warp owns
+    static constexpr int EC = EPI_COLS < 32 ? EPI_COLS : 32;  // epilogue columns per chunk
+    static constexpr int EPI_WARPS = 4 * SPLIT;
     static constexpr int STG_BYTES = 32 * EC * 2;  // one warp's staging buffer (32 rows)
-    static constexpr int STG_TOTAL = 4 * 2 * STG_BYTES;
+    static constexpr int STG_TOTAL = EPI_WARPS * 2 * STG_BYTES;
     static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN;
     static constexpr int ROW_A = BK * 2;  // operand row bytes = swizzle span
     static constexpr int SMEM_LIMIT = 232448;
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             dev::mbar_init(dev::smem_u32(&tfull[i]), 1);
-            dev::mbar_init(dev::smem_u32(&tempty[i]), 4);
+            dev::mbar_init(dev::smem_u32(&tempty[i]), C::EPI_WARPS);
         }
         dev::mbar_init(dev::smem_u32(drain), 1);
         *abort_flag = 0;
@@ -336,12 +340,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 record_error(kErrTimeoutDrain, abort_flag);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp - 4 < C::EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
         constexpr int EC = C::EC;
         constexpr int ROW_Y = EC * 2;
-        const int ew = warp & 3;  // this warp may access TMEM lanes [32*ew, 32*ew+32)
-        uint8_t *my_stg = sm_stg + ew * 2 * C::STG_BYTES;
+        const int ew = warp & 3;          // this warp may access TMEM lanes [32*ew, 32*ew+32)
+        const int ep = warp - 4;          // epilogue warp index
+        const int col_base = (ep >> 2) * C::EPI_COLS;  // this warp's columns of the tile
+        uint8_t *my_stg = sm_stg + ep * 2 * C::STG_BYTES;
         int sbuf = 0;
         int lt = 0;
         const int row = ew * 32 + lane;  // this thread's row of the tile (TMEM lane)
@@ -374,7 +380,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                       : nullptr;
             if (combine) {
                 int got = 1;
-                if (lane == 0) got = wait_flag_bounded(a.flags + slot * 4 + ew, abort_flag, kWaitTimeoutNs) ? 1 : 0;
+                if (lane == 0)
+                    got = wait_flag_bounded(a.flags + slot * kTcFlagsPerSlot + ep, abort_flag, kWaitTimeoutNs) ? 1 : 0;
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!got) {
                     if (lane == 0 && !*abort_flag) record_error(kErrTimeoutEpilogue, abort_flag);
@@ -382,9 +389,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 __threadfence();
             }
-            const uint32_t t_lane = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN);
+            const uint32_t t_lane =
+                tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN + col_base);
 #pragma unroll 1
-            for (int j = 0; j < BN / EC; ++j) {
+            for (int j = 0; j < C::EPI_COLS / EC; ++j) {
                 uint32_t v[EC];
 #pragma unroll
                 for (int q = 0; q < EC / 16; ++q)
@@ -392,7 +400,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 dev::tmem_ld_wait();
 #pragma unroll
                 for (int q = 0; q < EC / 16; ++q) dev::reg_fence16(v + q * 16);
-                if (j == BN / EC - 1) {
+                if (j == C::EPI_COLS / EC - 1) {
                     // The accumulator is in registers: hand the TMEM buffer back to the MMA warp.
                     dev::tc_fence_before_sync();
                     __syncwarp();
@@ -402,7 +410,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // Column-group-major, row-minor: a warp writes 512 contiguous bytes per store.
 #pragma unroll
                     for (int q = 0; q < EC / 4; ++q)
-                        __stcg(part + (size_t)(j * (EC / 4) + q) * C::BM + row,
+                        __stcg(part + (size_t)((col_base + j * EC) / 4 + q) * C::BM + row,
                                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
                     continue;
@@ -410,14 +418,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (combine) {
 #pragma unroll
                     for (int q = 0; q < EC / 4; ++q) {
-                        const float4 p4 = __ldcg(part + (size_t)(j * (EC / 4) + q) * C::BM + row);
+                        const float4 p4 = __ldcg(part + (size_t)((col_base + j * EC) / 4 + q) * C::BM + row);
                         v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) + p4.x);
                         v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + p4.y);
                         v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + p4.z);
                         v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + p4.w);
                     }
                 }
-                const int ch0 = n0 + j * EC;
+                const int ch0 = n0 + col_base + j * EC;
                 uint32_t packed[EC / 2];
                 if (ch0 + EC <= a.c_out) {
 #pragma unroll
@@ -464,10 +472,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // Every lane's partial sums are visible GPU-wide before the flag rises.
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) st_release_gpu(a.flags + slot * 4 + ew, 1);
+                if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 1);
             } else if (combine) {
                 __syncwarp();  // all lanes have read the partial: the slot is free again
-                if (lane == 0) st_release_gpu(a.flags + slot * 4 + ew, 0);
+                if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 0);
             }
         }
         if (lane == 0) dev::bulk_wait_group<0>();
@@ -554,9 +562,10 @@ cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, TcMaps *
                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
-    // y: (C_out, M), box (EC, 32): one epilogue warp's rows.
+    // y: (C_out, M), box (EC, 32): one epilogue warp's rows, one column chunk.
     {
-        const int ec = block_n < 64 ? block_n : 64;
+        int split = 1, ec = 16;
+        tc_epilogue_geometry(block_n, &split, &ec);
         cuuint64_t dims[2] = {(cuuint64_t)p.c_out, (cuuint64_t)p.m};
         cuuint64_t strides[1] = {(cuuint64_t)p.c_out * 2};
         cuuint32_t box[2] = {(cuuint32_t)ec, 32};
@@ -737,20 +746,25 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
 
 }  // namespace
 
+static int staging_bytes(int block_n)
+{
+    int split = 1, ec = 16;
+    tc_epilogue_geometry(block_n, &split, &ec);
+    return 4 * split * 2 * 32 * ec * 2;
+}
+
 int tc_smem_bytes(int block_n, int block_k, int stages)
 {
     const int a = (kTcBlockM * block_k * 2 + 1023) / 1024 * 1024;
     const int b = (block_n * block_k * 2 + 1023) / 1024 * 1024;
-    const int ec = block_n < 64 ? block_n : 64;
-    return 1024 + stages * (a + b) + 8 * 32 * ec * 2 + 256;
+    return 1024 + stages * (a + b) + staging_bytes(block_n) + 256;
 }
 
 static int stages_for(int block_n, int block_k)
 {
     const int a = (kTcBlockM * block_k * 2 + 1023) / 1024 * 1024;
     const int b = (block_n * block_k * 2 + 1023) / 1024 * 1024;
-    const int ec = block_n < 64 ? block_n : 64;
-    const int fit = (232448 - 1024 - 8 * 32 * ec * 2 - 256) / (a + b);
+    const int fit = (232448 - 1024 - staging_bytes(block_n) - 256) / (a + b);
     return fit < 8 ? fit : 8;
 }
 
@@ -815,7 +829,7 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
     t.flag_bytes = 0;
     if (t.stream_k) {
         t.grid = sm_count;
-        t.flag_bytes = ((long long)(t.grid - 1) * 4 * (long long)sizeof(int) + 255) / 256 * 256;
+        t.flag_bytes = ((long long)(t.grid - 1) * kTcFlagsPerSlot * (long long)sizeof(int) + 255) / 256 * 256;
         t.workspace_bytes = t.flag_bytes + (long long)(t.grid - 1) * kTcBlockM * t.block_n * 4;
     }
     return t;

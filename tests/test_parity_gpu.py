@@ -95,6 +95,13 @@ def test_layer_full_size_default_kernel(capi, name):
     assert_parity(y_to_f64(y), oracle_full(inp), f"{name} (auto)")
 
 
+@pytest.mark.parametrize("name", ["tiny", "down", "pointwise", "deep"])
+def test_layer_full_size_tcgen05_kernel(capi, name):
+    inp = make_layer_inputs(LAYERS[name])
+    y = run_gpu(capi, inp, algo="tcgen05")
+    assert_parity(y_to_f64(y), oracle_full(inp), f"{name} (tcgen05)")
+
+
 @pytest.mark.parametrize("name", ["tiny", "stem", "pointwise"])
 def test_layer_full_size_direct_kernel(capi, name):
     inp = make_layer_inputs(LAYERS[name])
@@ -149,9 +156,14 @@ SWEEP = [
 
 
 @pytest.mark.parametrize("case", SWEEP, ids=[str(i) for i in range(len(SWEEP))])
-@pytest.mark.parametrize("algo", ["auto", "direct"])
+@pytest.mark.parametrize("algo", ["auto", "direct", "tcgen05"])
 def test_shape_sweep(capi, case, algo):
     n, h, w, c, k, r, s, stride, pad = case
+    if algo == "tcgen05":
+        try:
+            capi.plan(n, h, w, c, k, r, s, stride, pad, "tcgen05")
+        except capi.CbsError:
+            pytest.skip("shape outside the tensor-core kernel")
     shape = LayerShape("sweep", n, h, w, c, k, r, s, 1, 0)
     inp = make_layer_inputs(shape, seed=1000 + hash(case) % 1000)
     y = run_gpu(capi, inp, algo=algo, stride=stride, pad=pad)
