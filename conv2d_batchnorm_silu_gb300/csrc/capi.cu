@@ -241,8 +241,8 @@ int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, in
     if (chosen == CBS_ALGO_TCGEN05) {
         if (!cbs::tc_supported(p)) return CBS_ERR_UNSUPPORTED;
         const cbs::TcPlan t = cbs::tc_make_plan(p, sm_count);
-        out.block_m = cbs::kTcBlockM;
-        out.block_n = t.block_n;
+        out.block_m = t.swap_ab ? t.block_n : cbs::kTcBlockM;  // output pixels per tile
+        out.block_n = t.swap_ab ? cbs::kTcBlockM : t.block_n;  // output channels per tile
         out.block_k = t.block_k;
         out.stages = t.stages;
         out.tiles = t.tiles;
@@ -251,6 +251,7 @@ int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, in
         out.smem_bytes = t.smem_bytes;
         out.k_iters = t.k_iters;
         out.stream_k = t.stream_k;
+        out.swap_ab = t.swap_ab;
         out.workspace_bytes = t.workspace_bytes;
     } else {
         const long long bx = (p.m + cbs::kDirectThreads - 1) / cbs::kDirectThreads;

@@ -170,7 +170,13 @@ __device__ __forceinline__ uint32_t swizzle_offset(uint32_t off)
     return off ^ (((off >> 7) & mask) << 4);
 }
 
-template <int BN, int BK>
+// SWAP = false: D[pixel][channel], A = im2col tile (128 pixels), B = weights (BN channels).
+// SWAP = true ("swap AB", for C_out <= 128): D[channel][pixel], A = weights (128
+// channels), B = im2col tile (BN = 256 pixels as two 128-pixel boxes), so the MMA
+// runs at N = 256 -- with operands streamed from shared memory an M=128 MMA costs
+// about the same time at N = 128 as at N = 256.  The epilogue transposes through
+// shared memory.
+template <int BN, int BK, bool SWAP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_conv_bn_silu_kernel(const __grid_constant__ CUtensorMap tm_x,
                            const __grid_constant__ CUtensorMap tm_w,
@@ -233,14 +239,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             WorkUnit u;
             while (!*abort_flag && wi.next(a, u)) {
                 const int m_tile = u.tile / a.n_tiles;
-                const int n0 = (u.tile - m_tile * a.n_tiles) * BN;
-                const int m0 = m_tile * C::BM;
+                const int n0 = (u.tile - m_tile * a.n_tiles) * (SWAP ? C::BM : BN);  // first channel
+                const int m0 = m_tile * (SWAP ? BN : C::BM);                        // first pixel
                 const int img = m0 / a.howo;
                 const int rem = m0 - img * a.howo;
                 const int oh = rem / a.wo;
                 const int ow = rem - oh * a.wo;
                 const int corner_w = ow * a.stride_w - a.pad_w;
                 const int corner_h = oh * a.stride_h - a.pad_h;
+                // SWAP: the second 128-pixel box of the tile (may lie past the last
+                // image: TMA then reads zeros).
+                const int m1 = m0 + C::BM;
+                const int img1 = m1 / a.howo;
+                const int rem1 = m1 - img1 * a.howo;
+                const int oh1 = rem1 / a.wo;
+                const int ow1 = rem1 - oh1 * a.wo;
+                const int corner_w1 = ow1 * a.stride_w - a.pad_w;
+                const int corner_h1 = oh1 * a.stride_h - a.pad_h;
                 int cc = u.kb % a.c_chunks;
                 int s = (u.kb / a.c_chunks) % a.s;
                 int r = (u.kb / a.c_chunks) / a.s;
@@ -254,11 +269,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     const uint32_t f_bar = dev::smem_u32(&full[stage]);
                     dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES + C::B_BYTES);
-                    dev::tma_load_im2col_4d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_x, f_bar,
-                                            cc * BK, corner_w, corner_h, img, (uint16_t)s,
-                                            (uint16_t)r);
-                    dev::tma_load_3d(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f_bar,
-                                     cc * BK, r * a.s + s, n0);
+                    if constexpr (SWAP) {
+                        dev::tma_load_3d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_w, f_bar,
+                                         cc * BK, r * a.s + s, n0);
+                        const uint32_t bdst = dev::smem_u32(sm_b + stage * C::B_STRIDE);
+                        dev::tma_load_im2col_4d(bdst, &tm_x, f_bar, cc * BK, corner_w, corner_h, img,
+                                                (uint16_t)s, (uint16_t)r);
+                        dev::tma_load_im2col_4d(bdst + C::BM * BK * 2, &tm_x, f_bar, cc * BK, corner_w1,
+                                                corner_h1, img1, (uint16_t)s, (uint16_t)r);
+                    } else {
+                        dev::tma_load_im2col_4d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_x, f_bar,
+                                                cc * BK, corner_w, corner_h, img, (uint16_t)s,
+                                                (uint16_t)r);
+                        dev::tma_load_3d(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f_bar,
+                                         cc * BK, r * a.s + s, n0);
+                    }
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++cc == a.c_chunks) {
@@ -368,6 +393,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             dev::tc_fence_after_sync();
+            if constexpr (SWAP) {
+                // TMEM lane = output channel, column = pixel.  Each thread owns one
+                // channel, so BN scale/bias are per-thread constants; the tile is
+                // transposed to NHWC through shared memory, 32 pixels x 32 channels
+                // per TMA store.
+                const int p_tile = u.tile / a.n_tiles;
+                const int ch_w0 = (u.tile - p_tile * a.n_tiles) * C::BM + ew * 32;  // warp's first channel
+                const int ch = ch_w0 + lane;
+                const float hs = ch < a.c_out ? 0.5f * __ldg(a.scale + ch) : 0.f;
+                const float hb = ch < a.c_out ? 0.5f * __ldg(a.bias + ch) : 0.f;
+                const int px_base = p_tile * BN + col_base;
+                const uint32_t t_lane =
+                    tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN + col_base);
+#pragma unroll 1
+                for (int j = 0; j < C::EPI_COLS / EC; ++j) {
+                    uint32_t v[EC];
+#pragma unroll
+                    for (int q = 0; q < EC / 16; ++q)
+                        dev::tmem_ld_32x32b_x16(t_lane + (uint32_t)(j * EC + q * 16), v + q * 16);
+                    dev::tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < EC / 16; ++q) dev::reg_fence16(v + q * 16);
+                    if (j == C::EPI_COLS / EC - 1) {
+                        dev::tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
+                    }
+                    if (lane == 0) dev::bulk_wait_group_read<1>();
+                    __syncwarp();
+                    __nv_bfloat16 *sb = reinterpret_cast<__nv_bfloat16 *>(my_stg + sbuf * C::STG_BYTES);
+#pragma unroll
+                    for (int pp = 0; pp < EC; ++pp)  // row pp: 32 channels, one per lane
+                        sb[pp * 32 + lane] =
+                            __float2bfloat16_rn(dev::silu_from_half(fmaf(__uint_as_float(v[pp]), hs, hb)));
+                    dev::fence_proxy_async_shared();
+                    __syncwarp();
+                    const int px0 = px_base + j * EC;
+                    if (lane == 0 && px0 < a.m && ch_w0 < a.c_out) {
+                        dev::tma_store_2d(&tm_y, dev::smem_u32(sb), ch_w0, px0);
+                        dev::bulk_commit_group();
+                    }
+                    sbuf ^= 1;
+                }
+                continue;
+            }
             const int m_tile = u.tile / a.n_tiles;
             const int n0 = (u.tile - m_tile * a.n_tiles) * BN;
             const int row0 = m_tile * C::BM + ew * 32;  // first output pixel of this warp
@@ -527,7 +597,7 @@ struct TcMaps {
     CUtensorMap x, w, y;
 };
 
-cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, TcMaps *maps)
+cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swap, TcMaps *maps)
 {
     cudaError_t st = load_encoders();
     if (st != cudaSuccess) return st;
@@ -554,7 +624,7 @@ cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, TcMaps *
     {
         cuuint64_t dims[3] = {(cuuint64_t)p.c, (cuuint64_t)p.r * p.s, (cuuint64_t)p.c_out};
         cuuint64_t strides[2] = {(cuuint64_t)p.c * 2, (cuuint64_t)p.r * p.s * p.c * 2};
-        cuuint32_t box[3] = {(cuuint32_t)block_k, 1, (cuuint32_t)block_n};
+        cuuint32_t box[3] = {(cuuint32_t)block_k, 1, (cuuint32_t)(swap ? kTcBlockM : block_n)};
         cuuint32_t estr[3] = {1, 1, 1};
         CUresult r = g_encode_tiled(&maps->w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.w),
                                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw_k,
@@ -568,12 +638,13 @@ cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, TcMaps *
         tc_epilogue_geometry(block_n, &split, &ec);
         cuuint64_t dims[2] = {(cuuint64_t)p.c_out, (cuuint64_t)p.m};
         cuuint64_t strides[1] = {(cuuint64_t)p.c_out * 2};
-        cuuint32_t box[2] = {(cuuint32_t)ec, 32};
+        // Swap AB: 32 channels x `ec` pixels, unswizzled 64-byte rows.
+        cuuint32_t box[2] = {(cuuint32_t)(swap ? 32 : ec), (cuuint32_t)(swap ? ec : 32)};
         cuuint32_t estr[2] = {1, 1};
         CUresult r = g_encode_tiled(&maps->y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.y, dims, strides,
                                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                    swizzle_for_row_bytes(ec * 2), CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                                    swap ? CU_TENSOR_MAP_SWIZZLE_NONE : swizzle_for_row_bytes(ec * 2),
+                                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     return cudaSuccess;
@@ -584,11 +655,11 @@ cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, TcMaps *
 struct MapKey {
     const void *x, *w, *y;
     int dims[11];
-    int block_n, block_k, device;
+    int block_n, block_k, device, swap;
     bool operator==(const MapKey &o) const
     {
         if (x != o.x || w != o.w || y != o.y || block_n != o.block_n || block_k != o.block_k ||
-            device != o.device)
+            device != o.device || swap != o.swap)
             return false;
         for (int i = 0; i < 11; ++i)
             if (dims[i] != o.dims[i]) return false;
@@ -607,7 +678,7 @@ struct MapCache {
 
 MapCache g_map_cache;
 
-cudaError_t cached_maps(const ConvProblem &p, int block_n, int block_k, TcMaps *out)
+cudaError_t cached_maps(const ConvProblem &p, int block_n, int block_k, bool swap, TcMaps *out)
 {
     MapKey k{};
     k.x = p.x;
@@ -617,6 +688,7 @@ cudaError_t cached_maps(const ConvProblem &p, int block_n, int block_k, TcMaps *
     for (int i = 0; i < 11; ++i) k.dims[i] = d[i];
     k.block_n = block_n;
     k.block_k = block_k;
+    k.swap = swap ? 1 : 0;
     cudaError_t st = cudaGetDevice(&k.device);
     if (st != cudaSuccess) return st;
     {
@@ -628,7 +700,7 @@ cudaError_t cached_maps(const ConvProblem &p, int block_n, int block_k, TcMaps *
             }
         }
     }
-    st = encode_maps(p, block_n, block_k, out);
+    st = encode_maps(p, block_n, block_k, swap, out);
     if (st != cudaSuccess) return st;
     std::lock_guard<std::mutex> lock(g_map_cache.mu);
     const int slot = g_map_cache.next;
@@ -691,12 +763,12 @@ cudaError_t stream_k_workspace(cudaStream_t stream, size_t bytes, size_t flag_by
     return cudaSuccess;
 }
 
-template <int BN, int BK>
+template <int BN, int BK, bool SWAP>
 cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &maps, cudaStream_t stream,
                        void *caller_workspace)
 {
     using C = TcCfg<BN, BK>;
-    auto kern = tc_conv_bn_silu_kernel<BN, BK>;
+    auto kern = tc_conv_bn_silu_kernel<BN, BK, SWAP>;
     // The shared-memory opt-in is per function and device: done once per device.
     static std::mutex attr_mu;
     static unsigned long long attr_done = 0;  // bit per device ordinal (< 64)
@@ -811,6 +883,23 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
             }
         }
     }
+    // Swap AB for 65..128 output channels: the tile becomes 128 channels x 256
+    // pixels so that every MMA runs at N = 256.
+    const long long ptiles256 = (p.m + 255) / 256;
+    t.swap_ab = (p.c_out > 64 && p.c_out <= 128 && ptiles256 >= sm_count) ? 1 : 0;
+    if (t.swap_ab) {
+        t.block_n = 256;
+        t.stages = stages_for(256, t.block_k);
+        t.m_tiles = (int)ptiles256;
+        t.n_tiles = (p.c_out + kTcBlockM - 1) / kTcBlockM;
+        t.tiles = t.m_tiles * t.n_tiles;
+        t.grid = std::min(t.tiles, sm_count);
+        t.smem_bytes = tc_smem_bytes(256, t.block_k, t.stages);
+        t.stream_k = 0;
+        t.workspace_bytes = 0;
+        t.flag_bytes = 0;
+        return t;
+    }
     t.stages = stages_for(t.block_n, t.block_k);
     t.m_tiles = m_tiles;
     t.n_tiles = (p.c_out + t.block_n - 1) / t.block_n;
@@ -844,11 +933,18 @@ cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, c
                                      void *workspace)
 {
     TcMaps maps;
-    cudaError_t st = cached_maps(p, plan.block_n, plan.block_k, &maps);
+    cudaError_t st = cached_maps(p, plan.block_n, plan.block_k, plan.swap_ab != 0, &maps);
     if (st != cudaSuccess) return st;
+    if (plan.swap_ab) {
+        if (plan.block_n != 256) return cudaErrorInvalidConfiguration;
+        if (plan.block_k == 64) return launch_cfg<256, 64, true>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 32) return launch_cfg<256, 32, true>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 16) return launch_cfg<256, 16, true>(p, plan, maps, stream, workspace);
+        return cudaErrorInvalidConfiguration;
+    }
 #define CBS_TC_CASE(BN_, BK_) \
     if (plan.block_n == BN_ && plan.block_k == BK_)       \
-        return launch_cfg<BN_, BK_>(p, plan, maps, stream, workspace);
+        return launch_cfg<BN_, BK_, false>(p, plan, maps, stream, workspace);
     CBS_TC_CASE(16, 16) CBS_TC_CASE(16, 32) CBS_TC_CASE(16, 64)
     CBS_TC_CASE(32, 16) CBS_TC_CASE(32, 32) CBS_TC_CASE(32, 64)
     CBS_TC_CASE(64, 16) CBS_TC_CASE(64, 32) CBS_TC_CASE(64, 64)

@@ -138,6 +138,7 @@ typedef struct cbs_plan_info {
     int smem_bytes;   /* dynamic shared memory per CTA */
     int k_iters;      /* pipeline steps per tile */
     int stream_k;     /* 1 when the K steps of all tiles are split evenly over the grid */
+    int swap_ab;      /* 1 when the GEMM runs transposed: channels on the MMA's M side, pixels on N */
     long long workspace_bytes; /* library-held scratch for stream-K partial tiles (0 if none) */
 } cbs_plan_info;
 

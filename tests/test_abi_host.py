@@ -68,7 +68,9 @@ def test_plan_for_the_five_layers(lib):
         p = lib.plan(sh.n, sh.h, sh.w, sh.c, sh.k, sh.r, sh.s, sh.stride, sh.pad, "auto", 152)
         assert p["algo"] == expect_algo[name], (name, p)
         if p["algo"] == "tcgen05":
-            assert p["block_m"] == 128 and p["block_n"] % 16 == 0 and p["block_n"] <= 256
+            assert p["swap_ab"] == (1 if name == "down" else 0)
+            assert p["block_m"] == (256 if p["swap_ab"] else 128)
+            assert p["block_n"] % 16 == 0 and p["block_n"] <= 256
             assert p["block_n"] >= min(sh.k, 128)
             assert p["stream_k"] == (1 if name == "deep" else 0)
             if p["stream_k"]:
@@ -78,7 +80,7 @@ def test_plan_for_the_five_layers(lib):
             assert p["smem_bytes"] <= 232448
             assert p["stages"] >= 2
             assert p["k_iters"] == sh.r * sh.s * -(-sh.c // p["block_k"])
-            tiles = -(-sh.m // 128) * -(-sh.k // p["block_n"])
+            tiles = -(-sh.m // p["block_m"]) * -(-sh.k // p["block_n"])
             assert p["tiles"] == tiles
 
 

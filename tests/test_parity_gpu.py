@@ -275,3 +275,24 @@ def test_stream_k_split_tiles(capi, case):
     y2 = run_gpu(capi, inp)
     assert np.array_equal(torch_bf16_to_bits(y1), torch_bf16_to_bits(y2))
     assert_parity(y_to_f64(y1), oracle_full(inp), f"{case} (stream-K)")
+
+
+SWAP_AB_CASES = [
+    # n, h, w, c, k, r, s, stride, pad: 65..128 output channels, >= one 256-pixel tile per SM
+    (1, 210, 190, 16, 80, 3, 3, 1, 1),    # channel tail (80 of 128), ragged last pixel tile
+    (2, 280, 280, 64, 128, 3, 3, 2, 1),   # stride 2, 32-pixel last tile
+]
+
+
+@pytest.mark.parametrize("case", SWAP_AB_CASES, ids=["c80_ragged", "s2_c128"])
+def test_swap_ab_tiles(capi, case):
+    """Shapes planned as channels x pixels tiles (MMA at N = 256, transposing epilogue)."""
+    n, h, w, c, k, r, s, stride, pad = case
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = capi.plan(n, h, w, c, k, r, s, stride, pad, "auto", sms)
+    assert p["algo"] == "tcgen05" and p["swap_ab"] == 1, p
+    inp = make_layer_inputs(LayerShape("swap", n, h, w, c, k, r, s, stride, pad), seed=41)
+    y1 = run_gpu(capi, inp)
+    y2 = run_gpu(capi, inp)
+    assert np.array_equal(torch_bf16_to_bits(y1), torch_bf16_to_bits(y2))
+    assert_parity(y_to_f64(y1), oracle_full(inp), f"{case} (swap AB)")
