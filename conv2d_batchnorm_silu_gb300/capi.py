@@ -41,7 +41,7 @@ _f = ctypes.c_float
 class PlanInfo(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in (
         "algo", "block_m", "block_n", "block_k", "stages", "tiles", "grid", "threads",
-        "smem_bytes", "k_iters", "stream_k", "swap_ab")] + [("workspace_bytes", ctypes.c_longlong)]
+        "smem_bytes", "k_iters", "stream_k", "swap_ab", "cluster")] + [("workspace_bytes", ctypes.c_longlong)]
 
     def as_dict(self) -> dict:
         d = {name: getattr(self, name) for name, _ in self._fields_}

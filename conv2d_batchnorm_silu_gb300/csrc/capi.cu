@@ -245,13 +245,14 @@ int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, in
         out.block_n = t.swap_ab ? cbs::kTcBlockM : t.block_n;  // output channels per tile
         out.block_k = t.block_k;
         out.stages = t.stages;
-        out.tiles = t.tiles;
+        out.tiles = t.m_tiles * t.n_tiles;
         out.grid = t.grid;
         out.threads = cbs::kTcThreads;
         out.smem_bytes = t.smem_bytes;
         out.k_iters = t.k_iters;
         out.stream_k = t.stream_k;
         out.swap_ab = t.swap_ab;
+        out.cluster = t.pair ? 2 : 1;
         out.workspace_bytes = t.workspace_bytes;
     } else {
         const long long bx = (p.m + cbs::kDirectThreads - 1) / cbs::kDirectThreads;

@@ -31,6 +31,7 @@ struct TcPlan {
     int grid;
     int smem_bytes;
     int swap_ab;                  // 1: tile = 128 channels x block_n pixels, D = W * X^T
+    int pair;                     // 1: clusters of two CTAs share (multicast) each weight tile
     int stream_k;                 // 1: K steps split evenly over the grid (see tc_conv.cu)
     long long workspace_bytes;    // stream-K partial tiles + flags (0 when not split)
     long long flag_bytes;         // the leading part of the workspace that must start zeroed

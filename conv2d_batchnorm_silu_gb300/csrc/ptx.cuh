@@ -94,6 +94,33 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
         : "memory");
 }
 
+// Tiled 3-D load multicast to every CTA of the cluster in `cta_mask`: the data
+// lands at the same shared-memory offset in each, and each one's mbarrier at
+// offset `bar` receives the byte count.
+__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap *tm, uint32_t bar,
+                                                      int c0, int c1, int c2, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Full barrier across the CTAs of the cluster (every thread of each CTA takes part).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
 // Im2col 4-D load (tensor dims C, W, H, N): pixelsPerColumn output pixels
 // starting at window corner (w, h) of image n, each shifted by the filter
 // tap (off_w, off_h); channelsPerPixel channels from c.  Out-of-image
@@ -179,6 +206,16 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      bar)
                  : "memory");
+}
+
+// As tc_commit, arriving once on the mbarrier at offset `bar` in every CTA of the cluster in `cta_mask`.
+__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, shape from idesc.

@@ -62,8 +62,9 @@ struct WorkUnit {
     int tile, kb, ke;
 };
 
-// The units one CTA processes, in order.  Data-parallel: whole tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ...  Stream-K: the CTA's equal share [g, g_end) of the
+// The units one worker processes, in order.  A worker is a CTA, or a CTA pair
+// sharing one weight tile (PAIR).  Data-parallel: whole tiles vb, vb + vg, ...
+// Stream-K: the worker's equal share [g, g_end) of the
 // global K-step sequence (tile-major), cut at tile boundaries.  The host enables
 // stream-K only when every share is at least one tile long, so a unit is a whole
 // tile, the tail of a tile (kb > 0: the previous CTA holds its head) or the head
@@ -71,12 +72,15 @@ struct WorkUnit {
 struct WorkIter {
     long long g, g_end;
     int t;
-    __device__ explicit WorkIter(const TcArgs &a)
+    int stride;
+    // vb / vg: this worker's index and the worker count (a CTA, or a CTA pair).
+    __device__ WorkIter(const TcArgs &a, int vb, int vg)
     {
         const long long total = (long long)a.tiles * a.k_iters;
-        g = a.stream_k ? total * blockIdx.x / gridDim.x : 0;
-        g_end = a.stream_k ? total * (blockIdx.x + 1) / gridDim.x : 0;
-        t = blockIdx.x;
+        g = a.stream_k ? total * vb / vg : 0;
+        g_end = a.stream_k ? total * (vb + 1) / vg : 0;
+        t = vb;
+        stride = vg;
     }
     __device__ bool next(const TcArgs &a, WorkUnit &u)
     {
@@ -93,7 +97,7 @@ struct WorkIter {
         u.tile = t;
         u.kb = 0;
         u.ke = a.k_iters;
-        t += gridDim.x;
+        t += stride;
         return true;
     }
 };
@@ -176,7 +180,11 @@ __device__ __forceinline__ uint32_t swizzle_offset(uint32_t off)
 // runs at N = 256 -- with operands streamed from shared memory an M=128 MMA costs
 // about the same time at N = 128 as at N = 256.  The epilogue transposes through
 // shared memory.
-template <int BN, int BK, bool SWAP>
+// PAIR: the grid is launched as clusters of two CTAs that compute the two M
+// halves of a 256 x BN pair tile; each loads half of the weight tile and
+// multicasts it to both, halving the L2 traffic for B.  Each CTA keeps its own
+// M=128 MMAs and TMEM; both MMAs must release a stage before it is refilled.
+template <int BN, int BK, bool SWAP, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_conv_bn_silu_kernel(const __grid_constant__ CUtensorMap tm_x,
                            const __grid_constant__ CUtensorMap tm_w,
@@ -201,11 +209,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int rank = PAIR ? (int)dev::cluster_ctarank() : 0;  // M half of the pair tile
+    const int vb = PAIR ? (int)blockIdx.x >> 1 : (int)blockIdx.x;
+    const int vg = PAIR ? (int)gridDim.x >> 1 : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             dev::mbar_init(dev::smem_u32(&full[i]), 1);
-            dev::mbar_init(dev::smem_u32(&empty[i]), 1);
+            dev::mbar_init(dev::smem_u32(&empty[i]), PAIR ? 2 : 1);
         }
         for (int i = 0; i < 2; ++i) {
             dev::mbar_init(dev::smem_u32(&tfull[i]), 1);
@@ -226,6 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     dev::tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) dev::cluster_sync();  // the peer's barriers exist before any multicast
     dev::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -235,11 +247,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issued_parity = 0;
-            WorkIter wi(a);
+            WorkIter wi(a, vb, vg);
             WorkUnit u;
             while (!*abort_flag && wi.next(a, u)) {
-                const int m_tile = u.tile / a.n_tiles;
-                const int n0 = (u.tile - m_tile * a.n_tiles) * (SWAP ? C::BM : BN);  // first channel
+                const int m_unit = u.tile / a.n_tiles;
+                const int m_tile = PAIR ? 2 * m_unit + rank : m_unit;
+                const int n0 = (u.tile - m_unit * a.n_tiles) * (SWAP ? C::BM : BN);  // first channel
                 const int m0 = m_tile * (SWAP ? BN : C::BM);                        // first pixel
                 const int img = m0 / a.howo;
                 const int rem = m0 - img * a.howo;
@@ -281,8 +294,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         dev::tma_load_im2col_4d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_x, f_bar,
                                                 cc * BK, corner_w, corner_h, img, (uint16_t)s,
                                                 (uint16_t)r);
-                        dev::tma_load_3d(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f_bar,
-                                         cc * BK, r * a.s + s, n0);
+                        if constexpr (PAIR) {
+                            // This CTA's half of the weight rows, delivered to both CTAs.
+                            dev::tma_load_3d_multicast(
+                                dev::smem_u32(sm_b + stage * C::B_STRIDE) + rank * (BN / 2) * BK * 2, &tm_w,
+                                f_bar, cc * BK, r * a.s + s, n0 + rank * (BN / 2), (uint16_t)0x3);
+                        } else {
+                            dev::tma_load_3d(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f_bar,
+                                             cc * BK, r * a.s + s, n0);
+                        }
                     }
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -324,7 +344,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t phase = 0;
             int lt = 0;
             bool ok = true;
-            WorkIter wi(a);
+            WorkIter wi(a, vb, vg);
             WorkUnit u;
             for (; ok && wi.next(a, u); ++lt) {
                 const int buf = lt & 1;
@@ -350,7 +370,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int kk = 1; kk < BK / 16; ++kk)
                         dev::tc_mma_bf16(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, 1u);
-                    dev::tc_commit(dev::smem_u32(&empty[stage]));
+                    if constexpr (PAIR)
+                        dev::tc_commit_multicast(dev::smem_u32(&empty[stage]), (uint16_t)0x3);
+                    else
+                        dev::tc_commit(dev::smem_u32(&empty[stage]));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -376,7 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int sbuf = 0;
         int lt = 0;
         const int row = ew * 32 + lane;  // this thread's row of the tile (TMEM lane)
-        WorkIter wi(a);
+        WorkIter wi(a, vb, vg);
         WorkUnit u;
         for (; wi.next(a, u); ++lt) {
             const int buf = lt & 1;
@@ -438,14 +461,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 continue;
             }
-            const int m_tile = u.tile / a.n_tiles;
-            const int n0 = (u.tile - m_tile * a.n_tiles) * BN;
+            const int m_unit = u.tile / a.n_tiles;
+            const int m_tile = PAIR ? 2 * m_unit + rank : m_unit;
+            const int n0 = (u.tile - m_unit * a.n_tiles) * BN;
             const int row0 = m_tile * C::BM + ew * 32;  // first output pixel of this warp
             // Stream-K: the tail of a split tile leaves its fp32 partial sums for the
             // CTA holding the head, which adds them (in a fixed order) and finishes.
             const bool publish = u.kb > 0;
             const bool combine = u.ke < a.k_iters;
-            const int slot = publish ? (int)blockIdx.x - 1 : (int)blockIdx.x;
+            // Slot of the worker boundary; a pair keeps one partial tile per M half.
+            const int slot = (publish ? vb - 1 : vb) * (PAIR ? 2 : 1) + rank;
             float4 *part = a.stream_k ? reinterpret_cast<float4 *>(a.partial) + (size_t)slot * (32 * BN)
                                       : nullptr;
             if (combine) {
@@ -554,6 +579,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     dev::tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) dev::cluster_sync();  // no CTA leaves while its peer may still write to it
     if (warp == 1) {
         dev::tc_fence_after_sync();
         dev::tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -597,7 +623,7 @@ struct TcMaps {
     CUtensorMap x, w, y;
 };
 
-cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swap, TcMaps *maps)
+cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swap, bool pair, TcMaps *maps)
 {
     cudaError_t st = load_encoders();
     if (st != cudaSuccess) return st;
@@ -624,7 +650,10 @@ cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swa
     {
         cuuint64_t dims[3] = {(cuuint64_t)p.c, (cuuint64_t)p.r * p.s, (cuuint64_t)p.c_out};
         cuuint64_t strides[2] = {(cuuint64_t)p.c * 2, (cuuint64_t)p.r * p.s * p.c * 2};
-        cuuint32_t box[3] = {(cuuint32_t)block_k, 1, (cuuint32_t)(swap ? kTcBlockM : block_n)};
+        // Rows of one load: the whole N tile, the 128-channel A tile when swapped,
+        // or half the N tile when a CTA pair multicasts the two halves.
+        const int rows = swap ? kTcBlockM : (pair ? block_n / 2 : block_n);
+        cuuint32_t box[3] = {(cuuint32_t)block_k, 1, (cuuint32_t)rows};
         cuuint32_t estr[3] = {1, 1, 1};
         CUresult r = g_encode_tiled(&maps->w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.w),
                                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw_k,
@@ -655,11 +684,11 @@ cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swa
 struct MapKey {
     const void *x, *w, *y;
     int dims[11];
-    int block_n, block_k, device, swap;
+    int block_n, block_k, device, swap, pair;
     bool operator==(const MapKey &o) const
     {
         if (x != o.x || w != o.w || y != o.y || block_n != o.block_n || block_k != o.block_k ||
-            device != o.device || swap != o.swap)
+            device != o.device || swap != o.swap || pair != o.pair)
             return false;
         for (int i = 0; i < 11; ++i)
             if (dims[i] != o.dims[i]) return false;
@@ -678,7 +707,7 @@ struct MapCache {
 
 MapCache g_map_cache;
 
-cudaError_t cached_maps(const ConvProblem &p, int block_n, int block_k, bool swap, TcMaps *out)
+cudaError_t cached_maps(const ConvProblem &p, int block_n, int block_k, bool swap, bool pair, TcMaps *out)
 {
     MapKey k{};
     k.x = p.x;
@@ -689,6 +718,7 @@ cudaError_t cached_maps(const ConvProblem &p, int block_n, int block_k, bool swa
     k.block_n = block_n;
     k.block_k = block_k;
     k.swap = swap ? 1 : 0;
+    k.pair = pair ? 1 : 0;
     cudaError_t st = cudaGetDevice(&k.device);
     if (st != cudaSuccess) return st;
     {
@@ -700,7 +730,7 @@ cudaError_t cached_maps(const ConvProblem &p, int block_n, int block_k, bool swa
             }
         }
     }
-    st = encode_maps(p, block_n, block_k, swap, out);
+    st = encode_maps(p, block_n, block_k, swap, pair, out);
     if (st != cudaSuccess) return st;
     std::lock_guard<std::mutex> lock(g_map_cache.mu);
     const int slot = g_map_cache.next;
@@ -763,12 +793,12 @@ cudaError_t stream_k_workspace(cudaStream_t stream, size_t bytes, size_t flag_by
     return cudaSuccess;
 }
 
-template <int BN, int BK, bool SWAP>
+template <int BN, int BK, bool SWAP, bool PAIR>
 cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &maps, cudaStream_t stream,
                        void *caller_workspace)
 {
     using C = TcCfg<BN, BK>;
-    auto kern = tc_conv_bn_silu_kernel<BN, BK, SWAP>;
+    auto kern = tc_conv_bn_silu_kernel<BN, BK, SWAP, PAIR>;
     // The shared-memory opt-in is per function and device: done once per device.
     static std::mutex attr_mu;
     static unsigned long long attr_done = 0;  // bit per device ordinal (< 64)
@@ -812,8 +842,26 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
         a.flags = static_cast<int *>(ws);
         a.partial = reinterpret_cast<float *>(static_cast<char *>(ws) + plan.flag_bytes);
     }
-    kern<<<plan.grid, kTcThreads, C::SMEM, stream>>>(maps.x, maps.w, maps.y, a);
-    return cudaGetLastError();
+    if constexpr (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)plan.grid);
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = C::SMEM;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        st = cudaLaunchKernelEx(&cfg, kern, maps.x, maps.w, maps.y, a);
+        if (st != cudaSuccess) return st;
+        return cudaGetLastError();
+    } else {
+        kern<<<plan.grid, kTcThreads, C::SMEM, stream>>>(maps.x, maps.w, maps.y, a);
+        return cudaGetLastError();
+    }
 }
 
 }  // namespace
@@ -896,6 +944,7 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
         t.grid = std::min(t.tiles, sm_count);
         t.smem_bytes = tc_smem_bytes(256, t.block_k, t.stages);
         t.stream_k = 0;
+        t.pair = 0;
         t.workspace_bytes = 0;
         t.flag_bytes = 0;
         return t;
@@ -916,10 +965,17 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
                      : 0;
     t.workspace_bytes = 0;
     t.flag_bytes = 0;
+    t.pair = 0;
     if (t.stream_k) {
         t.grid = sm_count;
-        t.flag_bytes = ((long long)(t.grid - 1) * kTcFlagsPerSlot * (long long)sizeof(int) + 255) / 256 * 256;
-        t.workspace_bytes = t.flag_bytes + (long long)(t.grid - 1) * kTcBlockM * t.block_n * 4;
+        // Pairs of CTAs (clusters of two) share each 256-wide weight tile: the
+        // stream-K worker is then the pair, over pair tiles of 256 x 256.
+        const int pair_tiles = (t.m_tiles + 1) / 2 * t.n_tiles;
+        t.pair = (t.block_n == 256 && sm_count % 2 == 0 && pair_tiles >= sm_count / 2) ? 1 : 0;
+        if (t.pair) t.tiles = pair_tiles;  // the kernel's work units
+        const long long slots = t.pair ? (long long)(sm_count / 2 - 1) * 2 : (long long)(t.grid - 1);
+        t.flag_bytes = (slots * kTcFlagsPerSlot * (long long)sizeof(int) + 255) / 256 * 256;
+        t.workspace_bytes = t.flag_bytes + slots * kTcBlockM * t.block_n * 4;
     }
     return t;
 }
@@ -933,18 +989,25 @@ cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, c
                                      void *workspace)
 {
     TcMaps maps;
-    cudaError_t st = cached_maps(p, plan.block_n, plan.block_k, plan.swap_ab != 0, &maps);
+    cudaError_t st = cached_maps(p, plan.block_n, plan.block_k, plan.swap_ab != 0, plan.pair != 0, &maps);
     if (st != cudaSuccess) return st;
     if (plan.swap_ab) {
         if (plan.block_n != 256) return cudaErrorInvalidConfiguration;
-        if (plan.block_k == 64) return launch_cfg<256, 64, true>(p, plan, maps, stream, workspace);
-        if (plan.block_k == 32) return launch_cfg<256, 32, true>(p, plan, maps, stream, workspace);
-        if (plan.block_k == 16) return launch_cfg<256, 16, true>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 64) return launch_cfg<256, 64, true, false>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 32) return launch_cfg<256, 32, true, false>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 16) return launch_cfg<256, 16, true, false>(p, plan, maps, stream, workspace);
+        return cudaErrorInvalidConfiguration;
+    }
+    if (plan.pair) {
+        if (plan.block_n != 256) return cudaErrorInvalidConfiguration;
+        if (plan.block_k == 64) return launch_cfg<256, 64, false, true>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 32) return launch_cfg<256, 32, false, true>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 16) return launch_cfg<256, 16, false, true>(p, plan, maps, stream, workspace);
         return cudaErrorInvalidConfiguration;
     }
 #define CBS_TC_CASE(BN_, BK_) \
     if (plan.block_n == BN_ && plan.block_k == BK_)       \
-        return launch_cfg<BN_, BK_, false>(p, plan, maps, stream, workspace);
+        return launch_cfg<BN_, BK_, false, false>(p, plan, maps, stream, workspace);
     CBS_TC_CASE(16, 16) CBS_TC_CASE(16, 32) CBS_TC_CASE(16, 64)
     CBS_TC_CASE(32, 16) CBS_TC_CASE(32, 32) CBS_TC_CASE(32, 64)
     CBS_TC_CASE(64, 16) CBS_TC_CASE(64, 32) CBS_TC_CASE(64, 64)
