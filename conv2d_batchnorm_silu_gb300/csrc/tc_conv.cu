@@ -62,35 +62,72 @@ struct WorkUnit {
     int tile, kb, ke;
 };
 
-// The units one worker processes, in order.  A worker is a CTA, or a CTA pair
-// sharing one weight tile (PAIR).  Data-parallel: whole tiles vb, vb + vg, ...
-// Stream-K: the worker's equal share [g, g_end) of the
+// The units one worker processes.  A worker is a CTA, or a CTA pair sharing
+// one weight tile (PAIR).  Data-parallel: whole tiles vb, vb + vg, ...
+// Stream-K: the worker's equal share of the
 // global K-step sequence (tile-major), cut at tile boundaries.  The host enables
 // stream-K only when every share is at least one tile long, so a unit is a whole
 // tile, the tail of a tile (kb > 0: the previous CTA holds its head) or the head
 // of a tile (ke < k_iters: the next CTA holds its tail), never a middle piece.
 struct WorkIter {
-    long long g, g_end;
-    int t;
-    int stride;
+    // stream-K state: the worker's range is [tail piece][whole tiles][head piece];
+    // it is processed as tail, head, then whole tiles (see next()).
+    int state;
+    int t_tail, kb_tail;   // tail piece: K steps [kb_tail, k_iters) of tile t_tail (kb_tail > 0)
+    int t_head, ke_head;   // head piece: K steps [0, ke_head) of tile t_head (ke_head < k_iters)
+    int t_full, t_full_end;  // whole tiles [t_full, t_full_end)
+    // data-parallel state
+    int t, stride;
     // vb / vg: this worker's index and the worker count (a CTA, or a CTA pair).
     __device__ WorkIter(const TcArgs &a, int vb, int vg)
     {
-        const long long total = (long long)a.tiles * a.k_iters;
-        g = a.stream_k ? total * vb / vg : 0;
-        g_end = a.stream_k ? total * (vb + 1) / vg : 0;
+        state = 0;
         t = vb;
         stride = vg;
+        if (a.stream_k) {
+            const long long total = (long long)a.tiles * a.k_iters;
+            const long long g0 = total * vb / vg, g1 = total * (vb + 1) / vg;
+            const int t0 = (int)(g0 / a.k_iters);
+            const int kb0 = (int)(g0 - (long long)t0 * a.k_iters);
+            const int t1 = (int)((g1 - 1) / a.k_iters);
+            const int ke1 = (int)(g1 - (long long)t1 * a.k_iters);
+            t_tail = kb0 > 0 ? t0 : -1;
+            kb_tail = kb0;
+            t_head = ke1 < a.k_iters ? t1 : -1;
+            ke_head = ke1;
+            t_full = kb0 > 0 ? t0 + 1 : t0;
+            t_full_end = ke1 < a.k_iters ? t1 : t1 + 1;
+        }
     }
+    // Stream-K order: the tail piece first (its partial sums are published at
+    // once), then the head piece (whose combine needs the next worker's tail,
+    // published early), then whole tiles -- so the fix-up happens mid-kernel and
+    // the last epilogue is a plain one.
     __device__ bool next(const TcArgs &a, WorkUnit &u)
     {
         if (a.stream_k) {
-            if (g >= g_end) return false;
-            u.tile = (int)(g / a.k_iters);
-            u.kb = (int)(g - (long long)u.tile * a.k_iters);
-            const long long left = g_end - g;
-            u.ke = left < (long long)(a.k_iters - u.kb) ? u.kb + (int)left : a.k_iters;
-            g += u.ke - u.kb;
+            if (state == 0) {
+                state = 1;
+                if (t_tail >= 0) {
+                    u.tile = t_tail;
+                    u.kb = kb_tail;
+                    u.ke = a.k_iters;
+                    return true;
+                }
+            }
+            if (state == 1) {
+                state = 2;
+                if (t_head >= 0) {
+                    u.tile = t_head;
+                    u.kb = 0;
+                    u.ke = ke_head;
+                    return true;
+                }
+            }
+            if (t_full >= t_full_end) return false;
+            u.tile = t_full++;
+            u.kb = 0;
+            u.ke = a.k_iters;
             return true;
         }
         if (t >= a.tiles) return false;
