@@ -53,6 +53,37 @@ inline void tc_epilogue_geometry(int block_n, int *split, int *ec)
 constexpr int kDirectThreads = 128;
 constexpr int kDirectBlockN = 16;
 
+// Launches `kern` on `stream` with programmatic stream serialization (the
+// kernel may start while its predecessor drains; see grid_dependency_wait in
+// ptx.cuh) and, when cluster_x > 1, clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, int cluster_x, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = (unsigned)n;
+    cudaError_t st = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (st != cudaSuccess) return st;
+    return cudaGetLastError();
+}
+
 // Planning (host only, no GPU needed).
 bool tc_supported(const ConvProblem &p);
 TcPlan tc_make_plan(const ConvProblem &p, int sm_count);

@@ -15,6 +15,7 @@
 
 #include "cbs_internal.h"
 #include "epilogue.cuh"
+#include "ptx.cuh"
 
 namespace cbs {
 namespace {
@@ -37,6 +38,8 @@ __global__ void __launch_bounds__(kDirectThreads)
     direct_conv_bn_silu_kernel(const DirectArgs a)
 {
     __shared__ __align__(16) float wsm[QCH][KB];
+    dev::grid_dependency_wait();
+    dev::grid_dependents_launch();
     const long long m = (long long)blockIdx.x * kDirectThreads + threadIdx.x;
     const int k0 = blockIdx.y * KB;
     const bool active = m < a.m;
@@ -124,6 +127,8 @@ __global__ void __launch_bounds__(NT) direct_small_kernel(const DirectArgs a)
 {
     constexpr int TAPS = R * S * C;
     __shared__ __align__(16) float wsm[TAPS][KB];
+    dev::grid_dependency_wait();
+    dev::grid_dependents_launch();
     const int k0 = blockIdx.y * KB;
     for (int i = threadIdx.x; i < TAPS * KB; i += NT) {
         const int q = i / KB, j = i - (i / KB) * KB;
@@ -219,8 +224,8 @@ bool try_small(const ConvProblem &p, const DirectArgs &a, cudaStream_t stream, c
     if (bx > 0x7fffffffLL) return false;
     dim3 grid((unsigned)bx, (unsigned)((p.c_out + KB - 1) / KB));
     if (grid.y > 65535) return false;
-    direct_small_kernel<R, S, C, kSmallThreads><<<grid, kSmallThreads, 0, stream>>>(a);
-    *err = cudaGetLastError();
+    *err = launch_overlapped(direct_small_kernel<R, S, C, kSmallThreads>, grid, dim3(kSmallThreads), 0, stream,
+                             1, a);
     return true;
 }
 
@@ -261,8 +266,7 @@ cudaError_t direct_launch(const ConvProblem &p, cudaStream_t stream)
     if (bx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)bx, (unsigned)((p.c_out + KB - 1) / KB));
     if (grid.y > 65535) return cudaErrorInvalidConfiguration;
-    direct_conv_bn_silu_kernel<<<grid, kDirectThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_overlapped(direct_conv_bn_silu_kernel, grid, dim3(kDirectThreads), 0, stream, 1, a);
 }
 
 }  // namespace cbs

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "cbs_internal.h"
+#include "ptx.cuh"
 
 namespace cbs {
 namespace {
@@ -14,6 +15,8 @@ __global__ void bn_fold_kernel(const float *__restrict__ gamma, const float *__r
                                const float *__restrict__ mean, const float *__restrict__ var, float eps,
                                int c_out, float *__restrict__ scale, float *__restrict__ bias)
 {
+    dev::grid_dependency_wait();
+    dev::grid_dependents_launch();
     const int k = blockIdx.x * blockDim.x + threadIdx.x;
     if (k >= c_out) return;
     const double sc = (double)gamma[k] / sqrt((double)var[k] + (double)eps);
@@ -27,9 +30,8 @@ cudaError_t fold_launch(const float *gamma, const float *beta, const float *mean
                         float eps, int c_out, float *scale, float *bias, cudaStream_t stream)
 {
     const int threads = 128;
-    bn_fold_kernel<<<(c_out + threads - 1) / threads, threads, 0, stream>>>(gamma, beta, mean, var, eps,
-                                                                           c_out, scale, bias);
-    return cudaGetLastError();
+    return launch_overlapped(bn_fold_kernel, dim3((unsigned)((c_out + threads - 1) / threads)), dim3(threads), 0,
+                             stream, 1, gamma, beta, mean, var, eps, c_out, scale, bias);
 }
 
 }  // namespace cbs

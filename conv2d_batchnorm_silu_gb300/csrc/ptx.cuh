@@ -22,6 +22,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// ---------------------------------------------------------------- launch overlap
+// Programmatic dependent launch: a kernel launched after another on the same
+// stream may start before its predecessor finishes.  Each kernel calls
+// grid_dependency_wait() before its first global-memory access (everything
+// before it -- barrier set-up, TMEM allocation, tensor-map prefetch -- overlaps
+// the predecessor's tail) and grid_dependents_launch() to let its own successor
+// be scheduled early.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {

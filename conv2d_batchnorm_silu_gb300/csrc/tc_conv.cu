@@ -277,6 +277,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if constexpr (PAIR) dev::cluster_sync();  // the peer's barriers exist before any multicast
     dev::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Global memory is touched only after the preceding kernel has finished.
+    dev::grid_dependency_wait();
+    dev::grid_dependents_launch();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -879,26 +882,8 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
         a.flags = static_cast<int *>(ws);
         a.partial = reinterpret_cast<float *>(static_cast<char *>(ws) + plan.flag_bytes);
     }
-    if constexpr (PAIR) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)plan.grid);
-        cfg.blockDim = dim3(kTcThreads);
-        cfg.dynamicSmemBytes = C::SMEM;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        st = cudaLaunchKernelEx(&cfg, kern, maps.x, maps.w, maps.y, a);
-        if (st != cudaSuccess) return st;
-        return cudaGetLastError();
-    } else {
-        kern<<<plan.grid, kTcThreads, C::SMEM, stream>>>(maps.x, maps.w, maps.y, a);
-        return cudaGetLastError();
-    }
+    return launch_overlapped(kern, dim3((unsigned)plan.grid), dim3(kTcThreads), (size_t)C::SMEM, stream,
+                             PAIR ? 2 : 1, maps.x, maps.w, maps.y, a);
 }
 
 }  // namespace
