@@ -67,7 +67,7 @@ int make_problem(int n, int h, int w_in, int c, int c_out, int r, int s, int sh,
 int select_algo(const cbs::ConvProblem &p, int algo)
 {
     if (algo != CBS_ALGO_AUTO) return algo;
-    return cbs::tc_supported(p) ? CBS_ALGO_TCGEN05 : CBS_ALGO_DIRECT;
+    return cbs::tc_supported(p) || cbs::gather_supported(p) ? CBS_ALGO_TCGEN05 : CBS_ALGO_DIRECT;
 }
 
 int sm_count_current_device(int *count)
@@ -145,11 +145,18 @@ int conv_bn_silu_forward_noalloc(const void *x, const void *w, const float *scal
     p.bias = bias;
     p.y = y;
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
-    if (!cbs::tc_supported(p)) {
-        cudaError_t e = cbs::direct_launch(p, strm);  // needs no scratch
+    int sms = 0;
+    if (!cbs::tc_supported(p)) {  // neither of these kernels needs scratch
+        cudaError_t e;
+        if (cbs::gather_supported(p)) {
+            st = sm_count_current_device(&sms);
+            if (st != CBS_OK) return st;
+            e = cbs::gather_launch(p, sms, strm);
+        } else {
+            e = cbs::direct_launch(p, strm);
+        }
         return e == cudaSuccess ? CBS_OK : cuda_fail(e);
     }
-    int sms = 0;
     st = sm_count_current_device(&sms);
     if (st != CBS_OK) return st;
     const cbs::TcPlan plan = cbs::tc_make_plan(p, sms);
@@ -200,10 +207,14 @@ int conv_bn_silu_forward_algo(const void *x, const void *w, const float *scale, 
     const int chosen = select_algo(p, algo);
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     if (chosen == CBS_ALGO_TCGEN05) {
-        if (!cbs::tc_supported(p)) return CBS_ERR_UNSUPPORTED;
+        if (!cbs::tc_supported(p) && !cbs::gather_supported(p)) return CBS_ERR_UNSUPPORTED;
         int sms = 0;
         st = sm_count_current_device(&sms);
         if (st != CBS_OK) return st;
+        if (!cbs::tc_supported(p)) {
+            cudaError_t e = cbs::gather_launch(p, sms, strm);
+            return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+        }
         const cbs::TcPlan plan = cbs::tc_make_plan(p, sms);
         cudaError_t e = cbs::tc_launch(p, plan, strm);
         return e == cudaSuccess ? CBS_OK : cuda_fail(e);
@@ -238,8 +249,23 @@ int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, in
     const int chosen = select_algo(p, algo);
     cbs_plan_info out{};
     out.algo = chosen;
-    if (chosen == CBS_ALGO_TCGEN05) {
-        if (!cbs::tc_supported(p)) return CBS_ERR_UNSUPPORTED;
+    if (chosen == CBS_ALGO_TCGEN05 && !cbs::tc_supported(p)) {
+        if (!cbs::gather_supported(p)) return CBS_ERR_UNSUPPORTED;
+        // Thin-input kernel: one 128-pixel tile per MMA step, K zero-padded to 32 or 64.
+        const int taps = r * s * c;
+        const int n16 = (c_out + 15) / 16 * 16;
+        const long long tiles = (p.m + 127) / 128;
+        out.block_m = 128;
+        out.block_n = n16;
+        out.block_k = taps <= 32 ? 32 : 64;
+        out.stages = 4;
+        out.tiles = (int)tiles;
+        out.grid = (int)(tiles < 2LL * sm_count ? tiles : 2LL * sm_count);
+        out.threads = cbs::kGatherBlockThreads;
+        out.smem_bytes = 1024 + 4 * 128 * out.block_k * 2 + (n16 * out.block_k * 2 + 1023) / 1024 * 1024 + 256;
+        out.k_iters = 1;
+        out.cluster = 1;
+    } else if (chosen == CBS_ALGO_TCGEN05) {
         const cbs::TcPlan t = cbs::tc_make_plan(p, sm_count);
         out.block_m = t.swap_ab ? t.block_n : cbs::kTcBlockM;  // output pixels per tile
         out.block_n = t.swap_ab ? cbs::kTcBlockM : t.block_n;  // output channels per tile
@@ -276,6 +302,10 @@ int conv_bn_silu_check(void *stream)
     unsigned int word = 0;
     cudaError_t e = cbs::tc_read_and_clear_error(static_cast<cudaStream_t>(stream), &word);
     if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int gword = 0;
+    e = cbs::gather_read_and_clear_error(static_cast<cudaStream_t>(stream), &gword);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (gword != 0 && word == 0) return CBS_ERR_TIMEOUT;
     if (word == 0) return CBS_OK;
     // A kernel gave up mid-way: stream-K ready flags may be left raised.
     e = cbs::tc_reset_workspaces();

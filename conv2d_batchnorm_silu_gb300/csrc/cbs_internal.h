@@ -102,6 +102,13 @@ bool direct_small_available(int r, int s, int c);
 cudaError_t fold_launch(const float *gamma, const float *beta, const float *mean, const float *var,
                         float eps, int c_out, float *scale, float *bias, cudaStream_t stream);
 
+// Thin-input tensor-core kernel (tc_gather.cu): 3x3 filters over 1, 3 or 4
+// channels, at most 64 output channels.
+bool gather_supported(const ConvProblem &p);
+cudaError_t gather_launch(const ConvProblem &p, int sm_count, cudaStream_t stream);
+cudaError_t gather_read_and_clear_error(cudaStream_t stream, unsigned int *out);
+constexpr int kGatherBlockThreads = 288;
+
 // Device error words (one per kernel translation unit): read and clear, stream-ordered.
 cudaError_t tc_read_and_clear_error(cudaStream_t stream, unsigned int *out);
 // Re-zeroes the stream-K ready flags of every workspace the library holds (after a

@@ -953,10 +953,12 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
             }
         }
     }
-    // Swap AB for 65..128 output channels: the tile becomes 128 channels x 256
-    // pixels so that every MMA runs at N = 256.
+    // Swap AB for 65..256 output channels (unless the long-K path above took the
+    // 256-wide pixel-major tile): the tile becomes 128 channels x 256 pixels so
+    // that every MMA runs at N = 256.
     const long long ptiles256 = (p.m + 255) / 256;
-    t.swap_ab = (p.c_out > 64 && p.c_out <= 128 && ptiles256 >= sm_count) ? 1 : 0;
+    const bool long_k_wide = p.c_out > 128 && t.block_n == 256 && t.k_iters >= 16;
+    t.swap_ab = (p.c_out > 64 && p.c_out <= 256 && !long_k_wide && ptiles256 >= sm_count / 2) ? 1 : 0;
     if (t.swap_ab) {
         t.block_n = 256;
         t.stages = stages_for(256, t.block_k);

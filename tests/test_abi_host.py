@@ -62,20 +62,26 @@ def test_output_dims(lib):
 
 def test_plan_for_the_five_layers(lib):
     from conv2d_batchnorm_silu_gb300.synthetic import LAYERS
-    expect_algo = {"tiny": "tcgen05", "stem": "direct", "down": "tcgen05",
+    expect_algo = {"tiny": "tcgen05", "stem": "tcgen05", "down": "tcgen05",
                    "pointwise": "tcgen05", "deep": "tcgen05"}
     for name, sh in LAYERS.items():
         p = lib.plan(sh.n, sh.h, sh.w, sh.c, sh.k, sh.r, sh.s, sh.stride, sh.pad, "auto", 152)
         assert p["algo"] == expect_algo[name], (name, p)
+        if name == "stem":
+            # thin-input tensor-core kernel: K = 27 zero-padded to 32, two CTAs per SM
+            assert p["block_m"] == 128 and p["block_n"] == 16 and p["block_k"] == 32
+            assert p["tiles"] == 800 and p["grid"] == 304 and p["smem_bytes"] <= 113 * 1024
+            continue
         if p["algo"] == "tcgen05":
-            assert p["swap_ab"] == (1 if name == "down" else 0)
+            assert p["swap_ab"] == (1 if name in ("down", "pointwise") else 0)
             assert p["block_m"] == (256 if p["swap_ab"] else 128)
             assert p["block_n"] % 16 == 0 and p["block_n"] <= 256
             assert p["block_n"] >= min(sh.k, 128)
             assert p["stream_k"] == (1 if name == "deep" else 0)
             if p["stream_k"]:
                 assert p["block_n"] == 256 and p["grid"] == 152
-                assert p["workspace_bytes"] >= 151 * 128 * 256 * 4
+                assert p["cluster"] == 2
+                assert p["workspace_bytes"] >= 150 * 128 * 256 * 4
             assert p["grid"] <= 152 and p["grid"] <= p["tiles"]
             assert p["smem_bytes"] <= 232448
             assert p["stages"] >= 2
@@ -86,8 +92,10 @@ def test_plan_for_the_five_layers(lib):
 
 def test_plan_rejects_what_tcgen05_cannot_run(lib):
     with pytest.raises(lib.CbsError) as e:
-        lib.plan(1, 64, 64, 3, 16, 3, 3, 2, 1, "tcgen05", 152)   # c = 3: 6-byte pixel stride
+        lib.plan(1, 64, 64, 5, 16, 3, 3, 2, 1, "tcgen05", 152)   # c = 5: neither TMA nor gather
     assert e.value.status == lib.CBS_ERR_UNSUPPORTED
+    # a 3-channel stem is taken by the thin-input tensor-core kernel
+    assert lib.plan(1, 64, 64, 3, 16, 3, 3, 2, 1, "tcgen05", 152)["algo"] == "tcgen05"
     with pytest.raises(lib.CbsError):
         lib.plan(1, 64, 64, 16, 12, 3, 3, 1, 1, "tcgen05", 152)  # c_out % 8 != 0
     assert lib.plan(1, 64, 64, 3, 16, 3, 3, 2, 1, "direct", 152)["algo"] == "direct"
@@ -114,7 +122,7 @@ def test_invalid_arguments_return_status_without_gpu(lib):
     assert f("conv_bn_silu_forward_algo", good, good, good, good, good, 1, 8, 8, 16, 16, 3, 3, 1, 1,
              1, 1, 7, None) == lib.CBS_ERR_INVALID_ARG
     # unsupported shape for a forced tcgen05 call, rejected before any launch
-    assert f("conv_bn_silu_forward_algo", good, good, good, good, good, 1, 8, 8, 3, 16, 3, 3, 1, 1,
+    assert f("conv_bn_silu_forward_algo", good, good, good, good, good, 1, 8, 8, 5, 16, 3, 3, 1, 1,
              1, 1, 1, None) == lib.CBS_ERR_UNSUPPORTED
     # empty batch / no output channels are no-ops even with null pointers
     assert f("conv_bn_silu_forward", None, None, None, None, None, 0, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1,

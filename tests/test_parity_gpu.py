@@ -146,7 +146,10 @@ SWEEP = [
     (3, 5, 5, 16, 8, 1, 1, 1, 0),       # c_out = 8 < smallest tile
     (1, 6, 6, 16, 16, 3, 3, 3, 0),      # stride larger than needed
     (1, 9, 9, 16, 16, 3, 3, 2, 0),      # no padding, stride 2
-    (2, 8, 8, 3, 16, 3, 3, 2, 1),       # 3-channel stem shape (direct kernel)
+    (2, 8, 8, 3, 16, 3, 3, 2, 1),       # 3-channel stem shape (thin-input tensor-core kernel)
+    (2, 13, 11, 4, 24, 3, 3, 1, 1),     # c = 4 (K 36 -> 64), c_out 24 in a 32-wide tile
+    (1, 30, 30, 1, 48, 3, 3, 2, 1),     # c = 1, N = 48
+    (1, 33, 17, 3, 64, 3, 3, 1, 0),     # c = 3, N = 64, no padding
     (1, 9, 7, 8, 8, 3, 3, 1, 1),        # c = 8 (direct)
     (2, 9, 7, 24, 20, 3, 3, 1, 1),      # c = 24, c_out = 20 (direct)
     (2, 9, 8, 16, 16, 3, 1, (1, 2), (1, 0)),  # asymmetric filter/stride/pad
@@ -278,13 +281,14 @@ def test_stream_k_split_tiles(capi, case):
 
 
 SWAP_AB_CASES = [
-    # n, h, w, c, k, r, s, stride, pad: 65..128 output channels, >= one 256-pixel tile per SM
+    # n, h, w, c, k, r, s, stride, pad: 65..256 output channels, many 256-pixel tiles
     (1, 210, 190, 16, 80, 3, 3, 1, 1),    # channel tail (80 of 128), ragged last pixel tile
     (2, 280, 280, 64, 128, 3, 3, 2, 1),   # stride 2, 32-pixel last tile
+    (1, 150, 150, 32, 200, 3, 3, 1, 1),   # two channel tiles, the second 72 wide
 ]
 
 
-@pytest.mark.parametrize("case", SWAP_AB_CASES, ids=["c80_ragged", "s2_c128"])
+@pytest.mark.parametrize("case", SWAP_AB_CASES, ids=["c80_ragged", "s2_c128", "c200_two_tiles"])
 def test_swap_ab_tiles(capi, case):
     """Shapes planned as channels x pixels tiles (MMA at N = 256, transposing epilogue)."""
     n, h, w, c, k, r, s, stride, pad = case
