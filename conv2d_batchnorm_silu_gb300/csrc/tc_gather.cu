@@ -140,20 +140,18 @@ __global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kern
     if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ producers
         const int row = (warp - 4) * 32 + lane;  // pixel of the tile this thread gathers
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int t = blockIdx.x; t < a.tiles && !*abort_flag; t += gridDim.x) {
+        // Receptive field of this thread's pixel in tile t: all loads issued at
+        // once (zeros in the padding).
+        auto gather = [&](int t, unsigned short (&v)[G::TAPS]) {
             const int m = t * 128 + row;
             int img = 0, oh = 0, ow = 0;
-            const bool active = m < a.m;
+            const bool active = t < a.tiles && m < a.m;
             if (active) {
                 img = m / a.howo;
                 const int rem = m - img * a.howo;
                 oh = rem / a.wo;
                 ow = rem - oh * a.wo;
             }
-            // All loads first, then packing: one memory latency per tile.
-            unsigned short v[G::TAPS];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
 #pragma unroll
@@ -167,6 +165,15 @@ __global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kern
                     for (int c = 0; c < C; ++c) v[(r * S + s) * C + c] = in ? __ldg(px + c) : (unsigned short)0;
                 }
             }
+        };
+        int stage = 0;
+        uint32_t phase = 0;
+        unsigned short cur[G::TAPS], nxt[G::TAPS];
+        gather(blockIdx.x, cur);
+        for (int t = blockIdx.x; t < a.tiles && !*abort_flag; t += gridDim.x) {
+            // Software pipeline: the next tile's loads are in flight while this
+            // tile is packed into shared memory.
+            gather(t + gridDim.x, nxt);
             int ok = 1;
             if (lane == 0)
                 ok = dev::mbar_wait_bounded(dev::smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
@@ -185,8 +192,8 @@ __global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kern
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int q = j * 8 + e * 2;
-                    const uint32_t lo = q < G::TAPS ? v[q < G::TAPS ? q : 0] : 0u;
-                    const uint32_t hi = q + 1 < G::TAPS ? v[q + 1 < G::TAPS ? q + 1 : 0] : 0u;
+                    const uint32_t lo = q < G::TAPS ? cur[q < G::TAPS ? q : 0] : 0u;
+                    const uint32_t hi = q + 1 < G::TAPS ? cur[q + 1 < G::TAPS ? q + 1 : 0] : 0u;
                     wv[e] = lo | (hi << 16);
                 }
                 *reinterpret_cast<uint4 *>(arow + swz<ROW>((uint32_t)(row * ROW + j * 16))) =
@@ -199,6 +206,8 @@ __global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kern
                 stage = 0;
                 phase ^= 1u;
             }
+#pragma unroll
+            for (int q = 0; q < G::TAPS; ++q) cur[q] = nxt[q];
         }
     } else if (warp == 8) {
         // ------------------------------------------------------------ MMA issuer
