@@ -75,6 +75,8 @@ def parse_args(argv=None):
                     help="comma-separated subset of layers in the step (default: all five)")
     ap.add_argument("--iso-iters", type=int, default=30,
                     help="calls per layer for the per-layer (L2-flushed) timings")
+    ap.add_argument("--no-unfused", action="store_true",
+                    help="skip the fused-vs-unfused comparison (conv, BN and SiLU as three kernels)")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch through the API each step instead of replaying CUDA graphs")
     args = ap.parse_args(argv)
@@ -384,6 +386,9 @@ def run_ours(args, rank, world, local_rank):
                 "peak_source": f"{peak_src} ({'bf16 dense burst' if bound == 'tensor' else 'HBM copy'})",
                 **per_launch}
 
+    fusion = None if args.no_unfused else \
+        fusion_comparison(capi, sets, layers, stream, dev, args.iso_iters, iso)
+
     e2e = run_e2e(args, capi, inputs, dev, stream, world) if args.e2e_steps > 0 else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -406,6 +411,7 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world} (each rank runs the full step)"},
         "roofline": roofline,
         "per_layer": per_layer,
+        "fusion": fusion,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
@@ -439,6 +445,47 @@ def isolated_layer_times(capi, sets, layers, stream, dev, iters) -> dict:
             out[n] = 1e3 * statistics.median(a.elapsed_time(b) for a, b in evs)
     del flush
     return out
+
+
+def fusion_comparison(capi, sets, layers, stream, dev, iters, fused_us) -> dict:
+    """The fused forward against the three-kernel sequence it replaces (conv -> t1,
+    BN -> t2, SiLU -> y), each layer timed alone like the fused one: L2 flushed
+    before every call, CUDA events around the whole sequence.  The unfused
+    sequence moves four extra copies of the output through HBM (t1 written and
+    read, t2 written and read)."""
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    out = {}
+    with torch.cuda.stream(stream):
+        for n in layers:
+            sh = LAYERS[n]
+            t1 = torch.empty((sh.n, sh.ho, sh.wo, sh.k), dtype=torch.bfloat16, device=dev)
+            t2 = torch.empty_like(t1)
+            evs = []
+            for i in range(iters):
+                lb = sets[i % ROTATION][n]
+                flush.zero_()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                capi.forward_unfused(lb.x, lb.w, lb.scale, lb.bias, sh.stride, sh.pad, y=lb.y,
+                                     t1=t1, t2=t2, stream=stream)
+                b.record(stream)
+                evs.append((a, b))
+            torch.cuda.synchronize()
+            capi.check(stream)
+            un_us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in evs)
+            y_bytes = 2 * sh.m * sh.k
+            out[n] = {"fused_us": round(fused_us[n], 3), "unfused_us": round(un_us, 3),
+                      "speedup": round(un_us / fused_us[n], 3),
+                      "hbm_bytes_fused": sh.compulsory_bytes,
+                      "hbm_bytes_unfused": sh.compulsory_bytes + 4 * y_bytes}
+            del t1, t2
+    del flush
+    tot_f = sum(v["fused_us"] for v in out.values())
+    tot_u = sum(v["unfused_us"] for v in out.values())
+    return {"layers": out, "fused_us_total": round(tot_f, 3), "unfused_us_total": round(tot_u, 3),
+            "speedup_total": round(tot_u / tot_f, 3),
+            "timing": "median of isolated calls, L2 flushed before each; unfused = 3 launches"}
 
 
 def run_e2e(args, capi, inputs, dev, stream, world):

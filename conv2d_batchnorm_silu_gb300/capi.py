@@ -60,6 +60,9 @@ _fold = _declare("conv_bn_silu_fold", [_p, _p, _p, _p, _f, _i, _p, _p, _p])
 _forward = _declare("conv_bn_silu_forward", [_p] * 5 + [_i] * 11 + [_p])
 _forward_algo = _declare("conv_bn_silu_forward_algo", [_p] * 5 + [_i] * 12 + [_p])
 _forward_noalloc = _declare("conv_bn_silu_forward_noalloc", [_p] * 5 + [_i] * 11 + [_p])
+_forward_unfused = _declare("conv_bn_silu_forward_unfused", [_p] * 7 + [_i] * 11 + [_p])
+_bn_apply = _declare("conv_bn_silu_bn_apply", [_p] * 4 + [ctypes.c_longlong, _i, _p])
+_silu_apply = _declare("conv_bn_silu_silu_apply", [_p, _p, ctypes.c_longlong, _p])
 _output_dims = _declare("conv_bn_silu_output_dims", [_i] * 8 + [ctypes.POINTER(_i)] * 2)
 _plan = _declare("conv_bn_silu_plan", [_i] * 13 + [ctypes.POINTER(PlanInfo)])
 _check = _declare("conv_bn_silu_check", [_p])
@@ -210,6 +213,75 @@ def forward_noalloc(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor, bias:
                           _dev_tensor(bias, torch.float32, "bias"), _dev_tensor(y, torch.bfloat16, "y"),
                           n, h, wi, c, c_out, r, s, sh, sw, ph, pw, _stream_handle(stream))
     _raise_if(st, "conv_bn_silu_forward_noalloc")
+    return y
+
+
+def forward_unfused(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor, bias: torch.Tensor,
+                    stride=1, pad=0, y: torch.Tensor | None = None, t1: torch.Tensor | None = None,
+                    t2: torch.Tensor | None = None, stream=None):
+    """conv_bn_silu_forward_unfused: the three-kernel sequence the fusion replaces.
+
+    conv -> t1 (bf16), BN -> t2 (bf16), SiLU -> y (bf16); t1, t2 and y are
+    allocated when not given.  Returns (y, t1, t2).  A comparator to measure
+    the fused forward against, not a replacement for it.
+    """
+    if x.dim() != 4 or w.dim() != 4:
+        raise ValueError("x must be NHWC and w KRSC (4-D)")
+    n, h, wi, c = x.shape
+    c_out, r, s, c2 = w.shape
+    if c2 != c:
+        raise ValueError(f"channel mismatch: x has {c}, w has {c2}")
+    if scale.numel() != c_out or bias.numel() != c_out:
+        raise ValueError("scale and bias must have c_out elements")
+    sh, sw = _pair(stride)
+    ph, pw = _pair(pad)
+    ho, wo = output_dims(h, wi, r, s, (sh, sw), (ph, pw))
+    shape = (n, ho, wo, c_out)
+    out = []
+    for t in (y, t1, t2):
+        if t is None:
+            t = torch.empty(shape, dtype=torch.bfloat16, device=x.device)
+        elif tuple(t.shape) != shape:
+            raise ValueError(f"output has shape {tuple(t.shape)}, expected {shape}")
+        out.append(t)
+    y, t1, t2 = out
+    if y.numel() == 0:
+        return y, t1, t2
+    st = _forward_unfused(_dev_tensor(x, torch.bfloat16, "x"), _dev_tensor(w, torch.bfloat16, "w"),
+                          _dev_tensor(scale, torch.float32, "scale"),
+                          _dev_tensor(bias, torch.float32, "bias"), _dev_tensor(t1, torch.bfloat16, "t1"),
+                          _dev_tensor(t2, torch.bfloat16, "t2"), _dev_tensor(y, torch.bfloat16, "y"),
+                          n, h, wi, c, c_out, r, s, sh, sw, ph, pw, _stream_handle(stream))
+    _raise_if(st, "conv_bn_silu_forward_unfused")
+    return y, t1, t2
+
+
+def bn_apply(t1: torch.Tensor, scale: torch.Tensor, bias: torch.Tensor,
+             t2: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """conv_bn_silu_bn_apply: t2 = bf16(t1 * scale[k] + bias[k]), k the innermost (channel) index."""
+    c_out = scale.numel()
+    if bias.numel() != c_out or t1.shape[-1] != c_out:
+        raise ValueError("t1's innermost dimension, scale and bias must all have c_out elements")
+    if t2 is None:
+        t2 = torch.empty_like(t1)
+    if t1.numel() == 0:
+        return t2
+    st = _bn_apply(_dev_tensor(t1, torch.bfloat16, "t1"), _dev_tensor(scale, torch.float32, "scale"),
+                   _dev_tensor(bias, torch.float32, "bias"), _dev_tensor(t2, torch.bfloat16, "t2"),
+                   t1.numel(), c_out, _stream_handle(stream))
+    _raise_if(st, "conv_bn_silu_bn_apply")
+    return t2
+
+
+def silu_apply(t2: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """conv_bn_silu_silu_apply: y = bf16(SiLU(t2)), elementwise."""
+    if y is None:
+        y = torch.empty_like(t2)
+    if t2.numel() == 0:
+        return y
+    st = _silu_apply(_dev_tensor(t2, torch.bfloat16, "t2"), _dev_tensor(y, torch.bfloat16, "y"),
+                     t2.numel(), _stream_handle(stream))
+    _raise_if(st, "conv_bn_silu_silu_apply")
     return y
 
 

@@ -94,6 +94,27 @@ int sm_count_current_device(int *count)
     return CBS_OK;
 }
 
+// Validated problem (pointers set) -> the chosen kernel's launch on `strm`.
+int launch_forward(const cbs::ConvProblem &p, int algo, cudaStream_t strm)
+{
+    const int chosen = select_algo(p, algo);
+    if (chosen == CBS_ALGO_TCGEN05) {
+        if (!cbs::tc_supported(p) && !cbs::gather_supported(p)) return CBS_ERR_UNSUPPORTED;
+        int sms = 0;
+        const int st = sm_count_current_device(&sms);
+        if (st != CBS_OK) return st;
+        if (!cbs::tc_supported(p)) {
+            cudaError_t e = cbs::gather_launch(p, sms, strm);
+            return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+        }
+        const cbs::TcPlan plan = cbs::tc_make_plan(p, sms);
+        cudaError_t e = cbs::tc_launch(p, plan, strm);
+        return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+    }
+    cudaError_t e = cbs::direct_launch(p, strm);
+    return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+}
+
 // ------------------------------------------------------------------ allocation-free forward
 // Scratch for conv_bn_silu_forward_noalloc: the stream-K partial tiles and ready
 // flags live in this fixed device array instead of library-allocated memory.
@@ -204,22 +225,57 @@ int conv_bn_silu_forward_algo(const void *x, const void *w, const float *scale, 
     p.scale = scale;
     p.bias = bias;
     p.y = y;
-    const int chosen = select_algo(p, algo);
+    return launch_forward(p, algo, static_cast<cudaStream_t>(stream));
+}
+
+int conv_bn_silu_forward_unfused(const void *x, const void *w, const float *scale, const float *bias,
+                                 void *t1, void *t2, void *y, int n, int h, int w_in, int c, int c_out,
+                                 int r, int s, int stride_h, int stride_w, int pad_h, int pad_w,
+                                 void *stream)
+{
+    cbs::ConvProblem p{};
+    int st = make_problem(n, h, w_in, c, c_out, r, s, stride_h, stride_w, pad_h, pad_w, &p);
+    if (st != CBS_OK) return st;
+    if (p.m == 0 || c_out == 0) return CBS_OK;
+    if (!x || !w || !scale || !bias || !t1 || !t2 || !y) return CBS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(scale) || !aligned16(bias) || !aligned16(t1) ||
+        !aligned16(t2) || !aligned16(y))
+        return CBS_ERR_MISALIGNED;
+    p.x = x;
+    p.w = w;
+    p.scale = scale;
+    p.bias = bias;
+    p.y = t1;
+    p.conv_only = 1;
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
-    if (chosen == CBS_ALGO_TCGEN05) {
-        if (!cbs::tc_supported(p) && !cbs::gather_supported(p)) return CBS_ERR_UNSUPPORTED;
-        int sms = 0;
-        st = sm_count_current_device(&sms);
-        if (st != CBS_OK) return st;
-        if (!cbs::tc_supported(p)) {
-            cudaError_t e = cbs::gather_launch(p, sms, strm);
-            return e == cudaSuccess ? CBS_OK : cuda_fail(e);
-        }
-        const cbs::TcPlan plan = cbs::tc_make_plan(p, sms);
-        cudaError_t e = cbs::tc_launch(p, plan, strm);
-        return e == cudaSuccess ? CBS_OK : cuda_fail(e);
-    }
-    cudaError_t e = cbs::direct_launch(p, strm);
+    st = launch_forward(p, CBS_ALGO_AUTO, strm);
+    if (st != CBS_OK) return st;
+    const long long count = p.m * c_out;
+    cudaError_t e = cbs::bn_apply_launch(t1, scale, bias, t2, count, c_out, strm);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cbs::silu_apply_launch(t2, y, count, strm);
+    return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+}
+
+int conv_bn_silu_bn_apply(const void *t1, const float *scale, const float *bias, void *t2,
+                          long long count, int c_out, void *stream)
+{
+    if (count < 0 || c_out < 1 || count % c_out != 0) return CBS_ERR_INVALID_ARG;
+    if (count > (1LL << 40)) return CBS_ERR_INVALID_ARG;
+    if (count == 0) return CBS_OK;
+    if (!t1 || !scale || !bias || !t2) return CBS_ERR_INVALID_ARG;
+    if (!aligned16(t1) || !aligned16(scale) || !aligned16(bias) || !aligned16(t2)) return CBS_ERR_MISALIGNED;
+    cudaError_t e = cbs::bn_apply_launch(t1, scale, bias, t2, count, c_out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+}
+
+int conv_bn_silu_silu_apply(const void *t2, void *y, long long count, void *stream)
+{
+    if (count < 0 || count > (1LL << 40)) return CBS_ERR_INVALID_ARG;
+    if (count == 0) return CBS_OK;
+    if (!t2 || !y) return CBS_ERR_INVALID_ARG;
+    if (!aligned16(t2) || !aligned16(y)) return CBS_ERR_MISALIGNED;
+    cudaError_t e = cbs::silu_apply_launch(t2, y, count, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CBS_OK : cuda_fail(e);
 }
 

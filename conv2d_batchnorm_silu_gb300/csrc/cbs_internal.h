@@ -17,7 +17,8 @@ struct ConvProblem {
     int n, h, w_in, c, c_out, r, s;
     int stride_h, stride_w, pad_h, pad_w;
     int ho, wo;
-    long long m;  // output pixels
+    long long m;    // output pixels
+    int conv_only;  // 1: store the bf16 convolution only (no BN, no SiLU) -- unfused comparator
 };
 
 // Tile configuration of the tcgen05 implicit GEMM.
@@ -99,6 +100,10 @@ cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, c
 cudaError_t direct_launch(const ConvProblem &p, cudaStream_t stream);
 // True when direct_launch has a fully unrolled variant for this filter shape.
 bool direct_small_available(int r, int s, int c);
+// Unfused comparator steps: t2 = BN(t1) and y = SiLU(t2), elementwise over NHWC bf16.
+cudaError_t bn_apply_launch(const void *t1, const float *scale, const float *bias, void *t2, long long count,
+                            int c_out, cudaStream_t stream);
+cudaError_t silu_apply_launch(const void *t2, void *y, long long count, cudaStream_t stream);
 cudaError_t fold_launch(const float *gamma, const float *beta, const float *mean, const float *var,
                         float eps, int c_out, float *scale, float *bias, cudaStream_t stream);
 

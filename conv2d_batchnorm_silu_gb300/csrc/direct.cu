@@ -32,6 +32,7 @@ struct DirectArgs {
     long long m;
     int h, w_in, c, c_out, r, s;
     int stride_h, stride_w, pad_h, pad_w, ho, wo;
+    int conv_only;  // 1: store the raw convolution (unfused comparator)
 };
 
 __global__ void __launch_bounds__(kDirectThreads)
@@ -102,9 +103,9 @@ __global__ void __launch_bounds__(kDirectThreads)
         uint32_t packed[KB / 2];
 #pragma unroll
         for (int j = 0; j < KB; j += 2)
-            packed[j / 2] = dev::pack_bf16x2(dev::bn_silu(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j)),
-                                             dev::bn_silu(acc[j + 1], __ldg(a.scale + k0 + j + 1),
-                                                          __ldg(a.bias + k0 + j + 1)));
+            packed[j / 2] = dev::pack_bf16x2(dev::epilogue_value(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j), a.conv_only),
+                                             dev::epilogue_value(acc[j + 1], __ldg(a.scale + k0 + j + 1),
+                                                                 __ldg(a.bias + k0 + j + 1), a.conv_only));
         uint4 *dst = reinterpret_cast<uint4 *>(yp);
 #pragma unroll
         for (int v = 0; v < KB / 8; ++v)
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kDirectThreads)
 #pragma unroll
         for (int j = 0; j < KB; ++j)
             if (k0 + j < a.c_out)
-                yp[j] = __float2bfloat16_rn(dev::bn_silu(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j)));
+                yp[j] = __float2bfloat16_rn(dev::epilogue_value(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j), a.conv_only));
     }
 }
 
@@ -199,9 +200,9 @@ __global__ void __launch_bounds__(NT) direct_small_kernel(const DirectArgs a)
         uint32_t packed[KB / 2];
 #pragma unroll
         for (int j = 0; j < KB; j += 2)
-            packed[j / 2] = dev::pack_bf16x2(dev::bn_silu(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j)),
-                                             dev::bn_silu(acc[j + 1], __ldg(a.scale + k0 + j + 1),
-                                                          __ldg(a.bias + k0 + j + 1)));
+            packed[j / 2] = dev::pack_bf16x2(dev::epilogue_value(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j), a.conv_only),
+                                             dev::epilogue_value(acc[j + 1], __ldg(a.scale + k0 + j + 1),
+                                                                 __ldg(a.bias + k0 + j + 1), a.conv_only));
         uint4 *dst = reinterpret_cast<uint4 *>(yp);
 #pragma unroll
         for (int v = 0; v < KB / 8; ++v)
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(NT) direct_small_kernel(const DirectArgs a)
 #pragma unroll
         for (int j = 0; j < KB; ++j)
             if (k0 + j < a.c_out)
-                yp[j] = __float2bfloat16_rn(dev::bn_silu(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j)));
+                yp[j] = __float2bfloat16_rn(dev::epilogue_value(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j), a.conv_only));
     }
 }
 
@@ -257,6 +258,7 @@ cudaError_t direct_launch(const ConvProblem &p, cudaStream_t stream)
     a.pad_w = p.pad_w;
     a.ho = p.ho;
     a.wo = p.wo;
+    a.conv_only = p.conv_only;
     cudaError_t err = cudaSuccess;
     if (try_small<3, 3, 1>(p, a, stream, &err) || try_small<3, 3, 3>(p, a, stream, &err) ||
         try_small<3, 3, 4>(p, a, stream, &err) || try_small<3, 3, 8>(p, a, stream, &err) ||

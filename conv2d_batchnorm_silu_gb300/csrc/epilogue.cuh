@@ -36,6 +36,14 @@ __device__ __forceinline__ float bn_silu(float acc, float scale, float bias)
     return silu_from_half(fmaf(acc, 0.5f * scale, 0.5f * bias));
 }
 
+// The fused epilogue, or (conv_only) the raw convolution output: the unfused
+// comparator's first step stores t1 = conv(x, W) and leaves BN and SiLU to
+// separate kernels.
+__device__ __forceinline__ float epilogue_value(float acc, float scale, float bias, int conv_only)
+{
+    return conv_only ? acc : bn_silu(acc, scale, bias);
+}
+
 // Two floats -> packed bf16x2 (round to nearest even), `lo` in the low half,
 // which is the lower address in memory.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)

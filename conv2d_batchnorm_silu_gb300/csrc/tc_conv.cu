@@ -52,6 +52,7 @@ struct TcArgs {
     int stride_h, stride_w, pad_h, pad_w;
     int s;
     int c_chunks, k_iters;
+    int conv_only;   // 1: store the raw convolution (unfused comparator)
     int stream_k;    // 1: each CTA takes an equal share of all K steps (see WorkIter)
     float *partial;  // stream-K: [grid-1][128*BN] fp32 partial tiles (slot c: boundary of CTAs c, c+1)
     int *flags;      // stream-K: [grid-1][8] ready flags, one per epilogue warp; 0 between launches
@@ -489,7 +490,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int pp = 0; pp < EC; ++pp)  // row pp: 32 channels, one per lane
                         sb[pp * 32 + lane] =
-                            __float2bfloat16_rn(dev::silu_from_half(fmaf(__uint_as_float(v[pp]), hs, hb)));
+                            __float2bfloat16_rn(a.conv_only ? __uint_as_float(v[pp])
+                                                            : dev::silu_from_half(fmaf(__uint_as_float(v[pp]), hs, hb)));
                     dev::fence_proxy_async_shared();
                     __syncwarp();
                     const int px0 = px_base + j * EC;
@@ -567,11 +569,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int i = 0; i < EC; i += 4) {
                         const float4 sc = __ldg(reinterpret_cast<const float4 *>(a.scale + ch0 + i));
                         const float4 bi = __ldg(reinterpret_cast<const float4 *>(a.bias + ch0 + i));
-                        packed[i / 2] = dev::pack_bf16x2(dev::bn_silu(__uint_as_float(v[i]), sc.x, bi.x),
-                                                         dev::bn_silu(__uint_as_float(v[i + 1]), sc.y, bi.y));
+                        packed[i / 2] = dev::pack_bf16x2(
+                            dev::epilogue_value(__uint_as_float(v[i]), sc.x, bi.x, a.conv_only),
+                            dev::epilogue_value(__uint_as_float(v[i + 1]), sc.y, bi.y, a.conv_only));
                         packed[i / 2 + 1] =
-                            dev::pack_bf16x2(dev::bn_silu(__uint_as_float(v[i + 2]), sc.z, bi.z),
-                                             dev::bn_silu(__uint_as_float(v[i + 3]), sc.w, bi.w));
+                            dev::pack_bf16x2(dev::epilogue_value(__uint_as_float(v[i + 2]), sc.z, bi.z, a.conv_only),
+                                             dev::epilogue_value(__uint_as_float(v[i + 3]), sc.w, bi.w, a.conv_only));
                     }
                 } else {
 #pragma unroll
@@ -581,8 +584,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const float b0 = c0 < a.c_out ? __ldg(a.bias + c0) : 0.f;
                         const float s1 = c1 < a.c_out ? __ldg(a.scale + c1) : 0.f;
                         const float b1 = c1 < a.c_out ? __ldg(a.bias + c1) : 0.f;
-                        packed[i / 2] = dev::pack_bf16x2(dev::bn_silu(__uint_as_float(v[i]), s0, b0),
-                                                         dev::bn_silu(__uint_as_float(v[i + 1]), s1, b1));
+                        packed[i / 2] = dev::pack_bf16x2(dev::epilogue_value(__uint_as_float(v[i]), s0, b0, a.conv_only),
+                                                         dev::epilogue_value(__uint_as_float(v[i + 1]), s1, b1, a.conv_only));
                     }
                 }
                 // Stage the warp's 32 rows x EC channels, then one TMA store.
@@ -870,6 +873,7 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
     a.s = p.s;
     a.c_chunks = plan.c_chunks;
     a.k_iters = plan.k_iters;
+    a.conv_only = p.conv_only;
     a.stream_k = plan.stream_k;
     a.partial = nullptr;
     a.flags = nullptr;

@@ -119,6 +119,42 @@ int conv_bn_silu_forward_noalloc(const void *x, const void *w, const float *scal
                                  void *y, int n, int h, int w_in, int c, int c_out, int r, int s,
                                  int stride_h, int stride_w, int pad_h, int pad_w, void *stream);
 
+/*
+ * Unfused comparator: the same layer as the three-kernel sequence that the
+ * fusion replaces -- the convolution writes t1 to memory, a BatchNorm kernel
+ * reads t1 and writes t2, a SiLU kernel reads t2 and writes y ("Fusing an
+ * Epilogue", kernels book, section "The problem": each step a round trip
+ * through memory; section "When not to fuse": measure the fused kernel
+ * against the sequence it replaces).  It exists to be measured against
+ * conv_bn_silu_forward, not to be used in its place.
+ *   t1 = bf16(conv2d(x, W))            (the forward kernel with the epilogue reduced to the cast)
+ *   t2 = bf16(t1 * scale[k] + bias[k])
+ *   y  = bf16(SiLU(t2))
+ * Arguments as conv_bn_silu_forward, plus
+ *   t1, t2 : device, bf16 NHWC [n][ho][wo][c_out] each, written (caller-owned
+ *            scratch; must not overlap each other or any other argument)
+ * y differs from conv_bn_silu_forward's by the two extra bf16 roundings of
+ * t1 and t2.  Three kernels are enqueued on `stream`.
+ */
+int conv_bn_silu_forward_unfused(const void *x, const void *w, const float *scale, const float *bias,
+                                 void *t1, void *t2, void *y, int n, int h, int w_in, int c, int c_out,
+                                 int r, int s, int stride_h, int stride_w, int pad_h, int pad_w,
+                                 void *stream);
+
+/* The comparator's BatchNorm step on its own, over `count` bf16 elements of
+ * an NHWC tensor with c_out channels (count % c_out == 0, count <= 2^40):
+ *   t2[i] = bf16(t1[i] * scale[i mod c_out] + bias[i mod c_out]), fp32 arithmetic.
+ * t1, t2: device bf16 [count]; scale, bias: device float32 [c_out]; all
+ * 16-byte aligned; t2 must not overlap the inputs.  count == 0 is a no-op. */
+int conv_bn_silu_bn_apply(const void *t1, const float *scale, const float *bias, void *t2,
+                          long long count, int c_out, void *stream);
+
+/* The comparator's SiLU step on its own: y[i] = bf16(SiLU(t2[i])) over `count`
+ * bf16 elements (count <= 2^40), SiLU(z) = z * sigmoid(z) in fp32 ("Fusing
+ * an Epilogue", section "The problem": SiLU is x times sigmoid of x).
+ * t2, y: device bf16 [count], 16-byte aligned, not overlapping. */
+int conv_bn_silu_silu_apply(const void *t2, void *y, long long count, void *stream);
+
 /* Output spatial size of the convolution; host only, touches no GPU.
  * ho = (h + 2*pad_h - r)/stride_h + 1, wo likewise; CBS_ERR_INVALID_ARG when
  * either would be < 1 or an argument is out of range. */

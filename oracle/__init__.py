@@ -128,14 +128,20 @@ def silu(z) -> np.ndarray:
         return z / (1.0 + np.exp(-z))
 
 
-def bn_silu(conv: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.ndarray:
-    """The epilogue of "The shape of it": z = acc*scale + bias, then SiLU(z).
+def bn(conv: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.ndarray:
+    """Folded inference BatchNorm: z = acc*scale + bias per output channel, float64.
 
+    ("Fusing an Epilogue", sections "The problem" and "The shape of it": batch
+    norm is a multiply and an add with one scale and one bias per channel.)
     ``conv`` has output channels last; scale/bias broadcast over them.
     """
-    z = np.asarray(conv, dtype=np.float64) * np.asarray(scale, np.float64) \
+    return np.asarray(conv, dtype=np.float64) * np.asarray(scale, np.float64) \
         + np.asarray(bias, np.float64)
-    return silu(z)
+
+
+def bn_silu(conv: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.ndarray:
+    """The epilogue of "The shape of it": z = acc*scale + bias, then SiLU(z)."""
+    return silu(bn(conv, scale, bias))
 
 
 def conv2d(x_bits: np.ndarray, w_bits: np.ndarray, stride=1, pad=0,

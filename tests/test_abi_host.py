@@ -129,6 +129,23 @@ def test_invalid_arguments_return_status_without_gpu(lib):
              None) == lib.CBS_OK
     assert f("conv_bn_silu_forward", None, None, None, None, None, 2, 8, 8, 16, 0, 3, 3, 1, 1, 1, 1,
              None) == lib.CBS_OK
+    # unfused comparator: t1/t2 are checked like y
+    uf = "conv_bn_silu_forward_unfused"
+    dims = (1, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1)
+    assert f(uf, good, good, good, good, None, good, good, *dims, None) == lib.CBS_ERR_INVALID_ARG
+    assert f(uf, good, good, good, good, good, odd, good, *dims, None) == lib.CBS_ERR_MISALIGNED
+    assert f(uf, None, None, None, None, None, None, None, 0, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1,
+             None) == lib.CBS_OK
+    bn_apply = lib._lib.conv_bn_silu_bn_apply
+    assert bn_apply(good, good, good, good, 100, 16, None) == lib.CBS_ERR_INVALID_ARG   # 100 % 16
+    assert bn_apply(good, good, good, good, 64, 0, None) == lib.CBS_ERR_INVALID_ARG
+    assert bn_apply(good, odd, good, good, 64, 16, None) == lib.CBS_ERR_MISALIGNED
+    assert bn_apply(None, None, None, None, 0, 16, None) == lib.CBS_OK
+    silu_apply = lib._lib.conv_bn_silu_silu_apply
+    assert silu_apply(good, good, -1, None) == lib.CBS_ERR_INVALID_ARG
+    assert silu_apply(good, None, 8, None) == lib.CBS_ERR_INVALID_ARG
+    assert silu_apply(odd, good, 8, None) == lib.CBS_ERR_MISALIGNED
+    assert silu_apply(None, None, 0, None) == lib.CBS_OK
     # fold: negative eps, null pointers, misaligned, c_out == 0
     fold = lib._lib.conv_bn_silu_fold
     assert fold(good, good, good, good, -1.0, 4, good, good, None) == lib.CBS_ERR_INVALID_ARG

@@ -96,6 +96,28 @@ def test_silu_against_mpmath():
         assert abs(g - ref) <= 4 * np.spacing(abs(ref)) + 1e-300, (z, g, ref)
 
 
+def test_bn_of_folded_statistics_is_batchnorm():
+    """oracle.bn with the folded scale/bias, channels last, equals the textbook
+    gamma*(t-mean)/sqrt(var+eps) + beta per channel (50 digits); at t = mean it is beta."""
+    rng = np.random.default_rng(4)
+    g = rng.uniform(0.5, 1.5, 6).astype(np.float32)
+    b = rng.normal(0, 0.1, 6).astype(np.float32)
+    m = rng.normal(0, 0.1, 6).astype(np.float32)
+    v = rng.uniform(0.5, 2, 6).astype(np.float32)
+    eps = np.float32(1e-3)
+    scale, bias = oracle.bn_fold(g, b, m, v, eps)
+    t = rng.normal(0, 2, (3, 4, 6))
+    got = oracle.bn(t, scale, bias)
+    assert got.shape == t.shape
+    for idx in np.ndindex(3, 4, 6):
+        k = idx[-1]
+        ref = (mpmath.mpf(float(g[k])) * (mpmath.mpf(float(t[idx])) - mpmath.mpf(float(m[k])))
+               / mpmath.sqrt(mpmath.mpf(float(v[k])) + mpmath.mpf(float(eps))) + mpmath.mpf(float(b[k])))
+        assert abs(got[idx] - float(ref)) <= 1e-14 * (1 + abs(float(ref))), idx
+    at_mean = oracle.bn(np.broadcast_to(m.astype(np.float64), (2, 6)), scale, bias)
+    np.testing.assert_allclose(at_mean, np.broadcast_to(b.astype(np.float64), (2, 6)), atol=1e-15)
+
+
 def test_bn_silu_per_channel_broadcast():
     """Channel k (last axis) uses scale[k] and bias[k]; identity BN gives SiLU(conv)."""
     conv = np.arange(2 * 3 * 5, dtype=np.float64).reshape(2, 3, 5) / 7.0 - 2.0

@@ -44,8 +44,8 @@ PY_MUTANTS = {
     "eps_dropped": ("scale = g / np.sqrt(v + e)", "scale = g / np.sqrt(v)"),
     "sigmoid_sign": ("return z / (1.0 + np.exp(-z))", "return z / (1.0 + np.exp(z))"),
     "plain_sigmoid": ("return z / (1.0 + np.exp(-z))", "return 1.0 / (1.0 + np.exp(-z))"),
-    "bias_before_scale": ("z = np.asarray(conv, dtype=np.float64) * np.asarray(scale, np.float64) \\\n        + np.asarray(bias, np.float64)",
-                          "z = (np.asarray(conv, dtype=np.float64) + np.asarray(bias, np.float64)) \\\n        * np.asarray(scale, np.float64)"),
+    "bias_before_scale": ("return np.asarray(conv, dtype=np.float64) * np.asarray(scale, np.float64) \\\n        + np.asarray(bias, np.float64)",
+                          "return (np.asarray(conv, dtype=np.float64) + np.asarray(bias, np.float64)) \\\n        * np.asarray(scale, np.float64)"),
 }
 
 
