@@ -32,7 +32,7 @@ struct TcPlan {
     int grid;
     int smem_bytes;
     int swap_ab;                  // 1: tile = 128 channels x block_n pixels, D = W * X^T
-    int pair;                     // 1: clusters of two CTAs share (multicast) each weight tile
+    int pair;                     // 1: clusters of two CTAs run the 2-CTA MMA, each holding half the weight tile
     int stream_k;                 // 1: K steps split evenly over the grid (see tc_conv.cu)
     long long workspace_bytes;    // stream-K partial tiles + flags (0 when not split)
     long long flag_bytes;         // the leading part of the workspace that must start zeroed
@@ -88,7 +88,8 @@ cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // Planning (host only, no GPU needed).
 bool tc_supported(const ConvProblem &p);
 TcPlan tc_make_plan(const ConvProblem &p, int sm_count);
-int tc_smem_bytes(int block_n, int block_k, int stages);
+// Dynamic shared memory of the tcgen05 kernel; `pair`: a 2-CTA pair holds half of each weight tile per CTA.
+int tc_smem_bytes(int block_n, int block_k, int stages, int pair);
 
 // Launchers; return cudaSuccess or the first CUDA error met.
 cudaError_t tc_launch(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream);

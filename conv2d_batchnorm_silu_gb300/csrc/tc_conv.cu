@@ -169,11 +169,12 @@ __device__ __forceinline__ bool wait_flag_bounded(const int *flag, const volatil
     }
 }
 
-template <int BN, int BK>
+// B_ROWS: weight (B) rows held per CTA -- BN, or BN/2 when a CTA pair splits them.
+template <int BN, int BK, int B_ROWS = BN>
 struct TcCfg {
     static constexpr int BM = kTcBlockM;
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int A_STRIDE = (A_BYTES + 1023) / 1024 * 1024;
     static constexpr int B_STRIDE = (B_BYTES + 1023) / 1024 * 1024;
     static constexpr int SPLIT = BN >= 64 ? 2 : 1;  // epilogue warps per TMEM lane quarter
@@ -218,17 +219,25 @@ __device__ __forceinline__ uint32_t swizzle_offset(uint32_t off)
 // runs at N = 256 -- with operands streamed from shared memory an M=128 MMA costs
 // about the same time at N = 128 as at N = 256.  The epilogue transposes through
 // shared memory.
-// PAIR: the grid is launched as clusters of two CTAs that compute the two M
-// halves of a 256 x BN pair tile; each loads half of the weight tile and
-// multicasts it to both, halving the L2 traffic for B.  Each CTA keeps its own
-// M=128 MMAs and TMEM; both MMAs must release a stage before it is refilled.
+// PAIR: the grid is launched as clusters of two CTAs that work as one on a
+// 256 x BN pair tile with the 2-CTA tensor-core MMA (tcgen05 cta_group::2,
+// M = 256): each CTA loads the A tile of its own 128 pixels and one half of
+// the weight tile (BN/2 channels), and holds the 128 x BN accumulator of its
+// pixels in its own TMEM.  Only the even CTA issues MMAs; the hardware feeds
+// both tensor cores from both CTAs' shared memory.  Per K step a CTA takes in
+// A + B/2 instead of A + B, and the smaller stages leave room for more of
+// them.  Both CTAs' loads complete on the even CTA's full barrier; its MMA
+// commits release the stage, and publish a finished accumulator, in both CTAs;
+// both CTAs' epilogue warps hand the accumulator back to the even CTA.
 template <int BN, int BK, bool SWAP, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_conv_bn_silu_kernel(const __grid_constant__ CUtensorMap tm_x,
                            const __grid_constant__ CUtensorMap tm_w,
                            const __grid_constant__ CUtensorMap tm_y, const TcArgs a)
 {
-    using C = TcCfg<BN, BK>;
+    static_assert(!(SWAP && PAIR), "CTA pairs serve the pixel-major (unswapped) tile only");
+    constexpr int CG = PAIR ? 2 : 1;  // tcgen05 CTA group
+    using C = TcCfg<BN, BK, PAIR ? BN / 2 : BN>;
     constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -254,11 +263,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             dev::mbar_init(dev::smem_u32(&full[i]), 1);
-            dev::mbar_init(dev::smem_u32(&empty[i]), PAIR ? 2 : 1);
+            dev::mbar_init(dev::smem_u32(&empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             dev::mbar_init(dev::smem_u32(&tfull[i]), 1);
-            dev::mbar_init(dev::smem_u32(&tempty[i]), C::EPI_WARPS);
+            // A pair's accumulator is released by the epilogue warps of both CTAs.
+            dev::mbar_init(dev::smem_u32(&tempty[i]), PAIR ? 2 * C::EPI_WARPS : C::EPI_WARPS);
         }
         dev::mbar_init(dev::smem_u32(drain), 1);
         *abort_flag = 0;
@@ -270,14 +280,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         dev::prefetch_tensormap(&tm_y);
     }
     if (warp == 1) {
-        dev::tmem_alloc(dev::smem_u32(tmem_slot), C::TMEM_COLS);
-        dev::tmem_relinquish_alloc_permit();
+        // CG = 2: collective over the pair (warp 1 of both CTAs); same columns in both.
+        dev::tmem_alloc<CG>(dev::smem_u32(tmem_slot), C::TMEM_COLS);
+        dev::tmem_relinquish_alloc_permit<CG>();
     }
     dev::tc_fence_before_sync();
     __syncthreads();
-    if constexpr (PAIR) dev::cluster_sync();  // the peer's barriers exist before any multicast
+    if constexpr (PAIR) dev::cluster_sync();  // the peer's barriers exist before any remote signal
     dev::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // PAIR: the even CTA's barriers that both CTAs signal, as shared::cluster addresses.
+    const uint32_t full0 = PAIR ? dev::mapa_cluster(dev::smem_u32(full), 0) : 0u;
+    const uint32_t tempty0 = PAIR ? dev::mapa_cluster(dev::smem_u32(tempty), 0) : 0u;
     // Global memory is touched only after the preceding kernel has finished.
     dev::grid_dependency_wait();
     dev::grid_dependents_launch();
@@ -322,8 +336,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     const uint32_t f_bar = dev::smem_u32(&full[stage]);
-                    dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES + C::B_BYTES);
-                    if constexpr (SWAP) {
+                    if constexpr (PAIR) {
+                        // Both CTAs' bytes complete on the even CTA's full barrier.
+                        if (rank == 0) dev::mbar_arrive_expect_tx(f_bar, 2 * (C::A_BYTES + C::B_BYTES));
+                        const uint32_t f0 = full0 + (uint32_t)(stage * 8);
+                        dev::tma_load_im2col_4d_pair(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_x, f0,
+                                                     cc * BK, corner_w, corner_h, img, (uint16_t)s,
+                                                     (uint16_t)r);
+                        dev::tma_load_3d_pair(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f0, cc * BK,
+                                              r * a.s + s, n0 + rank * (BN / 2));
+                    } else if constexpr (SWAP) {
+                        dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES + C::B_BYTES);
                         dev::tma_load_3d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_w, f_bar,
                                          cc * BK, r * a.s + s, n0);
                         const uint32_t bdst = dev::smem_u32(sm_b + stage * C::B_STRIDE);
@@ -332,18 +355,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         dev::tma_load_im2col_4d(bdst + C::BM * BK * 2, &tm_x, f_bar, cc * BK, corner_w1,
                                                 corner_h1, img1, (uint16_t)s, (uint16_t)r);
                     } else {
+                        dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES + C::B_BYTES);
                         dev::tma_load_im2col_4d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_x, f_bar,
                                                 cc * BK, corner_w, corner_h, img, (uint16_t)s,
                                                 (uint16_t)r);
-                        if constexpr (PAIR) {
-                            // This CTA's half of the weight rows, delivered to both CTAs.
-                            dev::tma_load_3d_multicast(
-                                dev::smem_u32(sm_b + stage * C::B_STRIDE) + rank * (BN / 2) * BK * 2, &tm_w,
-                                f_bar, cc * BK, r * a.s + s, n0 + rank * (BN / 2), (uint16_t)0x3);
-                        } else {
-                            dev::tma_load_3d(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f_bar,
-                                             cc * BK, r * a.s + s, n0);
-                        }
+                        dev::tma_load_3d(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f_bar,
+                                         cc * BK, r * a.s + s, n0);
                     }
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -361,11 +378,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (!ok) break;
             }
-            // Every load issued must land before the CTA may exit.
+            // Every load issued must land before the CTA may exit.  The odd CTA of a
+            // pair cannot see the full barrier its loads complete on; its loads have
+            // landed once the MMAs that read them released the stage.
             for (int i = 0; i < STAGES; ++i) {
                 if ((issued >> i) & 1u) {
-                    if (!dev::mbar_wait_bounded(dev::smem_u32(&full[i]), (issued_parity >> i) & 1u,
-                                                nullptr, kWaitTimeoutNs))
+                    const uint32_t bar = (PAIR && rank != 0) ? dev::smem_u32(&empty[i]) : dev::smem_u32(&full[i]);
+                    if (!dev::mbar_wait_bounded(bar, (issued_parity >> i) & 1u, nullptr, kWaitTimeoutNs))
                         record_error(kErrTimeoutDrain, abort_flag);
                 }
             }
@@ -373,8 +392,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = dev::idesc_bf16_f32(C::BM, BN);
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = dev::idesc_bf16_f32(PAIR ? 2 * C::BM : C::BM, BN);
             // Descriptors are built once; per stage and per K step only the start
             // address field (16-byte units, low bits) advances.  The single issuing
             // thread must spend almost nothing per MMA or it, not the tensor core,
@@ -407,24 +426,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     dev::tc_fence_after_sync();
                     const uint64_t da = desc_a0 + (uint64_t)(stage * (C::A_STRIDE >> 4));
                     const uint64_t db = desc_b0 + (uint64_t)(stage * (C::B_STRIDE >> 4));
-                    dev::tc_mma_bf16(d_tmem, da, db, idesc, it != u.kb ? 1u : 0u);
+                    dev::tc_mma_bf16<CG>(d_tmem, da, db, idesc, it != u.kb ? 1u : 0u);
 #pragma unroll
                     for (int kk = 1; kk < BK / 16; ++kk)
-                        dev::tc_mma_bf16(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, 1u);
+                        dev::tc_mma_bf16<CG>(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc,
+                                             1u);
                     if constexpr (PAIR)
-                        dev::tc_commit_multicast(dev::smem_u32(&empty[stage]), (uint16_t)0x3);
+                        dev::tc_commit_multicast<CG>(dev::smem_u32(&empty[stage]), (uint16_t)0x3);
                     else
-                        dev::tc_commit(dev::smem_u32(&empty[stage]));
+                        dev::tc_commit<CG>(dev::smem_u32(&empty[stage]));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                dev::tc_commit(dev::smem_u32(&tfull[buf]));
+                if constexpr (PAIR)
+                    dev::tc_commit_multicast<CG>(dev::smem_u32(&tfull[buf]), (uint16_t)0x3);
+                else
+                    dev::tc_commit<CG>(dev::smem_u32(&tfull[buf]));
             }
             // All MMAs issued by this thread must finish before TMEM is freed.
-            dev::tc_commit(dev::smem_u32(drain));
+            dev::tc_commit<CG>(dev::smem_u32(drain));
             if (!dev::mbar_wait_bounded(dev::smem_u32(drain), 0, nullptr, kWaitTimeoutNs))
                 record_error(kErrTimeoutDrain, abort_flag);
         }
@@ -541,7 +564,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // The accumulator is in registers: hand the TMEM buffer back to the MMA warp.
                     dev::tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
+                    if (lane == 0) {
+                        if (PAIR && rank != 0)
+                            dev::mbar_arrive_cluster(tempty0 + (uint32_t)(buf * 8));
+                        else
+                            dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
+                    }
                 }
                 if (publish) {
                     // Column-group-major, row-minor: a warp writes 512 contiguous bytes per store.
@@ -625,7 +653,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if constexpr (PAIR) dev::cluster_sync();  // no CTA leaves while its peer may still write to it
     if (warp == 1) {
         dev::tc_fence_after_sync();
-        dev::tmem_dealloc(tmem_base, C::TMEM_COLS);
+        dev::tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -694,7 +722,7 @@ cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swa
         cuuint64_t dims[3] = {(cuuint64_t)p.c, (cuuint64_t)p.r * p.s, (cuuint64_t)p.c_out};
         cuuint64_t strides[2] = {(cuuint64_t)p.c * 2, (cuuint64_t)p.r * p.s * p.c * 2};
         // Rows of one load: the whole N tile, the 128-channel A tile when swapped,
-        // or half the N tile when a CTA pair multicasts the two halves.
+        // or half the N tile per CTA of a 2-CTA pair.
         const int rows = swap ? kTcBlockM : (pair ? block_n / 2 : block_n);
         cuuint32_t box[3] = {(cuuint32_t)block_k, 1, (cuuint32_t)rows};
         cuuint32_t estr[3] = {1, 1, 1};
@@ -840,7 +868,7 @@ template <int BN, int BK, bool SWAP, bool PAIR>
 cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &maps, cudaStream_t stream,
                        void *caller_workspace)
 {
-    using C = TcCfg<BN, BK>;
+    using C = TcCfg<BN, BK, PAIR ? BN / 2 : BN>;
     auto kern = tc_conv_bn_silu_kernel<BN, BK, SWAP, PAIR>;
     // The shared-memory opt-in is per function and device: done once per device.
     static std::mutex attr_mu;
@@ -899,17 +927,17 @@ static int staging_bytes(int block_n)
     return 4 * split * 2 * 32 * ec * 2;
 }
 
-int tc_smem_bytes(int block_n, int block_k, int stages)
+int tc_smem_bytes(int block_n, int block_k, int stages, int pair)
 {
     const int a = (kTcBlockM * block_k * 2 + 1023) / 1024 * 1024;
-    const int b = (block_n * block_k * 2 + 1023) / 1024 * 1024;
+    const int b = ((pair ? block_n / 2 : block_n) * block_k * 2 + 1023) / 1024 * 1024;
     return 1024 + stages * (a + b) + staging_bytes(block_n) + 256;
 }
 
-static int stages_for(int block_n, int block_k)
+static int stages_for(int block_n, int block_k, int pair = 0)
 {
     const int a = (kTcBlockM * block_k * 2 + 1023) / 1024 * 1024;
-    const int b = (block_n * block_k * 2 + 1023) / 1024 * 1024;
+    const int b = ((pair ? block_n / 2 : block_n) * block_k * 2 + 1023) / 1024 * 1024;
     const int fit = (232448 - 1024 - staging_bytes(block_n) - 256) / (a + b);
     return fit < 8 ? fit : 8;
 }
@@ -970,7 +998,7 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
         t.n_tiles = (p.c_out + kTcBlockM - 1) / kTcBlockM;
         t.tiles = t.m_tiles * t.n_tiles;
         t.grid = std::min(t.tiles, sm_count);
-        t.smem_bytes = tc_smem_bytes(256, t.block_k, t.stages);
+        t.smem_bytes = tc_smem_bytes(256, t.block_k, t.stages, 0);
         t.stream_k = 0;
         t.pair = 0;
         t.workspace_bytes = 0;
@@ -982,7 +1010,7 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
     t.n_tiles = (p.c_out + t.block_n - 1) / t.block_n;
     t.tiles = t.m_tiles * t.n_tiles;
     t.grid = std::min(t.tiles, sm_count);
-    t.smem_bytes = tc_smem_bytes(t.block_n, t.block_k, t.stages);
+    t.smem_bytes = tc_smem_bytes(t.block_n, t.block_k, t.stages, 0);
     // Stream-K when whole tiles would leave a partly idle last wave: every CTA
     // takes total/grid consecutive K steps.  Each share must cover at least one
     // tile so that a tile is split between two CTAs at most.
@@ -996,11 +1024,16 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
     t.pair = 0;
     if (t.stream_k) {
         t.grid = sm_count;
-        // Pairs of CTAs (clusters of two) share each 256-wide weight tile: the
-        // stream-K worker is then the pair, over pair tiles of 256 x 256.
+        // Pairs of CTAs (clusters of two) run the 2-CTA MMA on pair tiles of
+        // 256 x 256, each CTA holding half of the weight tile: the stream-K worker
+        // is then the pair.
         const int pair_tiles = (t.m_tiles + 1) / 2 * t.n_tiles;
         t.pair = (t.block_n == 256 && sm_count % 2 == 0 && pair_tiles >= sm_count / 2) ? 1 : 0;
-        if (t.pair) t.tiles = pair_tiles;  // the kernel's work units
+        if (t.pair) {
+            t.tiles = pair_tiles;  // the kernel's work units
+            t.stages = stages_for(t.block_n, t.block_k, 1);
+            t.smem_bytes = tc_smem_bytes(t.block_n, t.block_k, t.stages, 1);
+        }
         const long long slots = t.pair ? (long long)(sm_count / 2 - 1) * 2 : (long long)(t.grid - 1);
         t.flag_bytes = (slots * kTcFlagsPerSlot * (long long)sizeof(int) + 255) / 256 * 256;
         t.workspace_bytes = t.flag_bytes + slots * kTcBlockM * t.block_n * 4;

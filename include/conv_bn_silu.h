@@ -175,7 +175,7 @@ typedef struct cbs_plan_info {
     int k_iters;      /* pipeline steps per tile */
     int stream_k;     /* 1 when the K steps of all tiles are split evenly over the grid */
     int swap_ab;      /* 1 when the GEMM runs transposed: channels on the MMA's M side, pixels on N */
-    int cluster;      /* CTAs per cluster: 2 when CTA pairs share (multicast) each weight tile */
+    int cluster;      /* CTAs per cluster: 2 when CTA pairs run the 2-CTA MMA, each holding half of every weight tile */
     long long workspace_bytes; /* library-held scratch for stream-K partial tiles (0 if none) */
 } cbs_plan_info;
 

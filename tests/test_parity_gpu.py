@@ -261,10 +261,11 @@ STREAM_K_CASES = [
     # n, h, w, c, k, r, s, stride, pad: more 128x256 tiles than SMs, K loop >= 16 steps
     (32, 20, 20, 128, 512, 3, 3, 1, 1),   # 200 tiles, 18 K steps
     (39, 20, 20, 256, 384, 3, 3, 1, 1),   # 244 tiles, ragged last M tile, a 128-channel N tail
+    (31, 20, 20, 128, 512, 3, 3, 1, 1),   # 97 M tiles: the last CTA pair's odd half is past the end
 ]
 
 
-@pytest.mark.parametrize("case", STREAM_K_CASES, ids=["200tiles", "244tiles_ragged"])
+@pytest.mark.parametrize("case", STREAM_K_CASES, ids=["200tiles", "244tiles_ragged", "odd_m_tiles"])
 def test_stream_k_split_tiles(capi, case):
     """Shapes whose plan splits the K loop of some tiles between two CTAs (stream-K):
     every output matches the oracle and two runs are bit-identical (the partial sums
