@@ -1,9 +1,10 @@
 #!/usr/bin/env python
 """Benchmark of the fused conv2d + BatchNorm + SiLU layer on GB300.
 
-One *step* is one pass of the whole hot path -- BN fold, then the fused
-forward -- over each of the five YOLO-shaped layers (tiny, stem, downsample,
-pointwise, deep), each on its own synthetic input.  ``value`` is the step's
+One *step* is one pass of the whole hot path over the five YOLO-shaped
+layers (tiny, stem, downsample, pointwise, deep), each on its own synthetic
+input: the BN fold of every layer (one batched launch), then each layer's
+fused forward.  ``value`` is the step's
 algorithmic work (2*M*C_out*C*R*S summed over the layers, padding not
 counted) divided by the device time of the timed steps, in TFLOP/s, summed
 over ranks (each rank runs its own replica: weak scaling, no collective on
@@ -14,7 +15,7 @@ launching stream, bracketed by a barrier and torch.cuda.synchronize() on
 both sides; max over ranks.  Inputs rotate over 3 buffer sets (about 426 MB
 touched per rotation, more than three times the 129 MB L2), so each step
 reads its data from HBM.  The step is replayed from CUDA graphs captured
-from the API calls (ten launches through Python per step would make the host
+from the API calls (six launches through Python per step would make the host
 the bottleneck); the dominant layer's forward is its own graph, so CUDA events
 on the stream bracket exactly that kernel inside the timed region.  Per-layer
 times in ``per_layer`` come from a separate pass with the L2 flushed before
@@ -49,8 +50,9 @@ from conv2d_batchnorm_silu_gb300.synthetic import (LAYERS, LAYER_ORDER,  # noqa:
 
 METRIC = "fused conv+BN+SiLU TFLOP/s and % of conv roofline on 1 GB300"
 UNIT = "TFLOP/s"
-WORKLOAD = ("five YOLO-shaped fused conv+BN+SiLU layers per step, each BN fold + fused forward once: "
-            "tiny 1x32x32x16->32 3x3s1p1, stem 1x640x640x3->16 3x3s2p1, "
+WORKLOAD = ("five YOLO-shaped fused conv+BN+SiLU layers per step: one batched BN fold of all "
+            "layers, then each fused forward once: tiny 1x32x32x16->32 3x3s1p1, "
+            "stem 1x640x640x3->16 3x3s2p1, "
             "down 16x160x160x64->128 3x3s2p1, pointwise 16x40x40x256->256 1x1, "
             "deep 32x20x20x512->512 3x3s1p1; NHWC bf16 x, KRSC bf16 W, fp32 BN")
 DOMINANT = "deep"
@@ -255,10 +257,10 @@ def run_ours(args, rank, world, local_rank):
     inputs = {name: make_layer_inputs(LAYERS[name]) for name in layers}
     sets = [{name: LayerBuffers(inputs[name], dev) for name in layers} for _ in range(ROTATION)]
     flops_step = sum(LAYERS[n].flops for n in layers)
-    launches_per_step = 2 * len(layers)
-
-    def fold_call(lb, strm):
-        capi.fold(lb.g, lb.b, lb.m, lb.v, lb.eps, lb.scale, lb.bias, stream=strm)
+    launches_per_step = 1 + len(layers)
+    # One batched BN fold per buffer set: every layer's scale and bias in one launch.
+    fold_batches = [capi.FoldBatch([(lb.g, lb.b, lb.m, lb.v, lb.eps, lb.scale, lb.bias)
+                                    for lb in (bufs[n] for n in layers)]) for bufs in sets]
 
     def forward_call(lb, strm):
         sh = lb.shape
@@ -266,10 +268,10 @@ def run_ours(args, rank, world, local_rank):
 
     # The step in launch order, split around the dominant layer's forward so that
     # CUDA events on the stream can bracket exactly that kernel.
-    def segments(bufs):
-        pre, post, dom, seen = [], [], None, False
+    def segments(i):
+        bufs = sets[i]
+        pre, post, dom, seen = [lambda s, fb=fold_batches[i]: fb(s)], [], None, False
         for name in layers:
-            (post if seen else pre).append(lambda s, lb=bufs[name]: fold_call(lb, s))
             if name == dominant:
                 seen = True
                 dom = (lambda s, lb=bufs[name]: forward_call(lb, s))
@@ -280,7 +282,7 @@ def run_ours(args, rank, world, local_rank):
     # Warm up through the API (first calls encode tensor maps and set kernel attributes).
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
-            pre, dom, post = segments(sets[i % ROTATION])
+            pre, dom, post = segments(i % ROTATION)
             for f in pre + [dom] + post:
                 f(stream)
     torch.cuda.synchronize()
@@ -289,7 +291,7 @@ def run_ours(args, rank, world, local_rank):
     # One CUDA graph per segment per buffer set.
     plan = []
     for i in range(ROTATION):
-        pre, dom, post = segments(sets[i])
+        pre, dom, post = segments(i)
         parts = []
         for calls in (pre, [dom], post):
             if not calls:
@@ -490,7 +492,7 @@ def fusion_comparison(capi, sets, layers, stream, dev, iters, fused_us) -> dict:
 
 def run_e2e(args, capi, inputs, dev, stream, world):
     """Same metric through the public API with host buffers: per step, every layer's x goes
-    host->device from pinned memory, the fold and fused forward run, and y comes back
+    host->device from pinned memory, the batched fold and the fused forwards run, and y comes back
     device->host into pinned memory.  Weights and BN statistics stay resident on the device."""
     layers = args.layers
     host_x = {n: bits_to_torch_bf16(inputs[n].x_bits).pin_memory() for n in layers}
@@ -500,13 +502,15 @@ def run_e2e(args, capi, inputs, dev, stream, world):
     d2h = sum(t.numel() * 2 for t in host_y.values())
     flops_step = sum(LAYERS[n].flops for n in layers)
 
+    fold = capi.FoldBatch([(b.g, b.b, b.m, b.v, b.eps, b.scale, b.bias) for b in (bufs[n] for n in layers)])
+
     def step():
         with torch.cuda.stream(stream):
+            fold(stream)
             for n in layers:
                 b = bufs[n]
                 sh = b.shape
                 b.x.copy_(host_x[n], non_blocking=True)
-                capi.fold(b.g, b.b, b.m, b.v, b.eps, b.scale, b.bias, stream=stream)
                 capi.forward(b.x, b.w, b.scale, b.bias, sh.stride, sh.pad, y=b.y, stream=stream)
                 host_y[n].copy_(b.y, non_blocking=True)
 
@@ -527,7 +531,7 @@ def run_e2e(args, capi, inputs, dev, stream, world):
     return {"value": round(aggregate_throughput(flops_step * args.e2e_steps, world, t) / 1e12, 3),
             "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(t / args.e2e_steps * 1e3, 4), "steps": args.e2e_steps,
-            "api": "conv2d_batchnorm_silu_gb300.capi.fold/forward on the C ABI, pinned host buffers"}
+            "api": "conv2d_batchnorm_silu_gb300.capi.FoldBatch/forward on the C ABI, pinned host buffers"}
 
 
 # ------------------------------------------------------------------ the oracle (CPU) legs

@@ -49,6 +49,12 @@ class PlanInfo(ctypes.Structure):
         return d
 
 
+class FoldLayer(ctypes.Structure):
+    """cbs_fold_layer: one layer of conv_bn_silu_fold_batch."""
+    _fields_ = [("gamma", _p), ("beta", _p), ("mean", _p), ("var", _p), ("eps", _f), ("c_out", _i),
+                ("scale", _p), ("bias", _p)]
+
+
 def _declare(name, argtypes, restype=ctypes.c_int):
     fn = getattr(_lib, name)
     fn.argtypes = argtypes
@@ -57,6 +63,7 @@ def _declare(name, argtypes, restype=ctypes.c_int):
 
 
 _fold = _declare("conv_bn_silu_fold", [_p, _p, _p, _p, _f, _i, _p, _p, _p])
+_fold_batch = _declare("conv_bn_silu_fold_batch", [ctypes.POINTER(FoldLayer), _i, _p])
 _forward = _declare("conv_bn_silu_forward", [_p] * 5 + [_i] * 11 + [_p])
 _forward_algo = _declare("conv_bn_silu_forward_algo", [_p] * 5 + [_i] * 12 + [_p])
 _forward_noalloc = _declare("conv_bn_silu_forward_noalloc", [_p] * 5 + [_i] * 11 + [_p])
@@ -148,6 +155,39 @@ def fold(gamma: torch.Tensor, beta: torch.Tensor, mean: torch.Tensor, var: torch
     _raise_if(_fold(ptrs[0], ptrs[1], ptrs[2], ptrs[3], float(eps), c_out, ptrs[4], ptrs[5],
                     _stream_handle(stream)), "conv_bn_silu_fold")
     return scale, bias
+
+
+class FoldBatch:
+    """A prepared conv_bn_silu_fold_batch call over fixed tensors (a network's layers):
+    the descriptor array is built once, each call() is one launch."""
+
+    def __init__(self, layers):
+        """layers: iterable of (gamma, beta, mean, var, eps, scale, bias); fp32 device tensors."""
+        layers = list(layers)
+        self._keep = layers
+        self._arr = (FoldLayer * max(1, len(layers)))()
+        for i, (g, b, m, v, eps, sc, bi) in enumerate(layers):
+            c_out = g.numel()
+            for t, nm in ((b, "beta"), (m, "mean"), (v, "var"), (sc, "scale"), (bi, "bias")):
+                if t.numel() != c_out:
+                    raise ValueError(f"layer {i}: {nm} has {t.numel()} elements, expected {c_out}")
+            self._arr[i] = FoldLayer(_dev_tensor(g, torch.float32, "gamma"), _dev_tensor(b, torch.float32, "beta"),
+                                     _dev_tensor(m, torch.float32, "mean"), _dev_tensor(v, torch.float32, "var"),
+                                     float(eps), c_out, _dev_tensor(sc, torch.float32, "scale"),
+                                     _dev_tensor(bi, torch.float32, "bias"))
+        self._n = len(layers)
+
+    def __call__(self, stream=None) -> None:
+        _raise_if(_fold_batch(self._arr, self._n, _stream_handle(stream)), "conv_bn_silu_fold_batch")
+
+
+def fold_batch(layers, stream=None) -> None:
+    """conv_bn_silu_fold_batch: every layer's BN fold in one launch.
+
+    layers: iterable of (gamma, beta, mean, var, eps, scale, bias) with fp32 device tensors;
+    scale and bias are written.
+    """
+    FoldBatch(layers)(stream)
 
 
 def forward(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor, bias: torch.Tensor,

@@ -208,6 +208,26 @@ int conv_bn_silu_fold(const float *gamma, const float *beta, const float *mean, 
     return e == cudaSuccess ? CBS_OK : cuda_fail(e);
 }
 
+int conv_bn_silu_fold_batch(const cbs_fold_layer *layers, int n_layers, void *stream)
+{
+    if (n_layers < 0 || (n_layers > 0 && !layers)) return CBS_ERR_INVALID_ARG;
+    std::vector<cbs::FoldLayer> v;
+    v.reserve((size_t)n_layers);
+    for (int i = 0; i < n_layers; ++i) {
+        const cbs_fold_layer &L = layers[i];
+        if (L.c_out < 0 || !(L.eps >= 0.0f) || L.eps > 3.0e38f) return CBS_ERR_INVALID_ARG;
+        if (L.c_out == 0) continue;
+        if (!L.gamma || !L.beta || !L.mean || !L.var || !L.scale || !L.bias) return CBS_ERR_INVALID_ARG;
+        if (!aligned16(L.gamma) || !aligned16(L.beta) || !aligned16(L.mean) || !aligned16(L.var) ||
+            !aligned16(L.scale) || !aligned16(L.bias))
+            return CBS_ERR_MISALIGNED;
+        v.push_back(cbs::FoldLayer{L.gamma, L.beta, L.mean, L.var, L.eps, L.c_out, L.scale, L.bias});
+    }
+    if (v.empty()) return CBS_OK;
+    cudaError_t e = cbs::fold_batch_launch(v.data(), (int)v.size(), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+}
+
 int conv_bn_silu_forward_algo(const void *x, const void *w, const float *scale, const float *bias,
                               void *y, int n, int h, int w_in, int c, int c_out, int r, int s,
                               int stride_h, int stride_w, int pad_h, int pad_w, int algo, void *stream)

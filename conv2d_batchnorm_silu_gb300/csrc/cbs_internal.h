@@ -40,7 +40,9 @@ struct TcPlan {
 
 constexpr int kTcBlockM = 128;
 constexpr int kTcThreads = 384;  // producer, MMA, two idle, eight epilogue warps
-constexpr int kTcFlagsPerSlot = 8;  // stream-K ready flags: one per epilogue warp
+// Stream-K slot words: a ready flag per epilogue warp, then an arrival ticket per epilogue warp.
+constexpr int kTcFlagsPerSlot = 16;
+constexpr int kTcTicketOffset = 8;
 
 // Epilogue geometry of the tensor-core kernel for an N tile of `block_n`
 // channels: `split` warps share each 32-row TMEM lane quarter (each takes
@@ -105,6 +107,20 @@ bool direct_small_available(int r, int s, int c);
 cudaError_t bn_apply_launch(const void *t1, const float *scale, const float *bias, void *t2, long long count,
                             int c_out, cudaStream_t stream);
 cudaError_t silu_apply_launch(const void *t2, void *y, long long count, cudaStream_t stream);
+// One layer of a batched BN fold (conv_bn_silu_fold_batch).
+struct FoldLayer {
+    const float *gamma, *beta, *mean, *var;
+    float eps;
+    int c_out;
+    float *scale, *bias;
+};
+constexpr int kFoldBatchMax = 16;  // layers per launch (kernel parameter space)
+struct FoldBatch {
+    FoldLayer layer[kFoldBatchMax];
+    int first_block[kFoldBatchMax];
+    int count;
+};
+cudaError_t fold_batch_launch(const FoldLayer *layers, int count, cudaStream_t stream);
 cudaError_t fold_launch(const float *gamma, const float *beta, const float *mean, const float *var,
                         float eps, int c_out, float *scale, float *bias, cudaStream_t stream);
 

@@ -55,7 +55,7 @@ struct TcArgs {
     int conv_only;   // 1: store the raw convolution (unfused comparator)
     int stream_k;    // 1: each CTA takes an equal share of all K steps (see WorkIter)
     float *partial;  // stream-K: [grid-1][128*BN] fp32 partial tiles (slot c: boundary of CTAs c, c+1)
-    int *flags;      // stream-K: [grid-1][8] ready flags, one per epilogue warp; 0 between launches
+    int *flags;      // stream-K: per slot, a ready flag and an arrival ticket per epilogue warp; 0 between launches
 };
 
 // K steps [kb, ke) of output tile `tile`.
@@ -100,10 +100,9 @@ struct WorkIter {
             t_full_end = ke1 < a.k_iters ? t1 : t1 + 1;
         }
     }
-    // Stream-K order: the tail piece first (its partial sums are published at
-    // once), then the head piece (whose combine needs the next worker's tail,
-    // published early), then whole tiles -- so the fix-up happens mid-kernel and
-    // the last epilogue is a plain one.
+    // Stream-K order: the tail piece first, then the head piece, then whole
+    // tiles -- the split pieces meet their other halves (computed early by the
+    // neighbouring workers, too) mid-kernel, and the last epilogue is a plain one.
     __device__ bool next(const TcArgs &a, WorkUnit &u)
     {
         if (a.stream_k) {
@@ -530,12 +529,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int m_tile = PAIR ? 2 * m_unit + rank : m_unit;
             const int n0 = (u.tile - m_unit * a.n_tiles) * BN;
             const int row0 = m_tile * C::BM + ew * 32;  // first output pixel of this warp
-            // Stream-K: the tail of a split tile leaves its fp32 partial sums for the
-            // CTA holding the head, which adds them (in a fixed order) and finishes.
-            const bool publish = u.kb > 0;
-            const bool combine = u.ke < a.k_iters;
-            // Slot of the worker boundary; a pair keeps one partial tile per M half.
-            const int slot = (publish ? vb - 1 : vb) * (PAIR ? 2 : 1) + rank;
+            // Stream-K: the two pieces of a split tile (the head of one worker's range
+            // and the tail of the next one's) meet in the slot of that worker boundary;
+            // a pair keeps one partial tile per M half.  Whichever piece's accumulator
+            // is ready first leaves its fp32 partial sums there; the other adds them
+            // and finishes the tile, so neither waits for the other to be computed.
+            // A sum of two fp32 values does not depend on their order: the result is
+            // the same whichever piece arrives first.
+            const bool split = a.stream_k && (u.kb > 0 || u.ke < a.k_iters);
+            const int slot = (u.kb > 0 ? vb - 1 : vb) * (PAIR ? 2 : 1) + rank;
+            bool publish = false, combine = false;
+            if (split) {
+                int first = 0;
+                if (lane == 0) first = atomicAdd(a.flags + slot * kTcFlagsPerSlot + kTcTicketOffset + ep, 1) == 0;
+                first = __shfl_sync(0xffffffffu, first, 0);
+                publish = first != 0;
+                combine = first == 0;
+            }
             float4 *part = a.stream_k ? reinterpret_cast<float4 *>(a.partial) + (size_t)slot * (32 * BN)
                                       : nullptr;
             if (combine) {
@@ -641,7 +651,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 1);
             } else if (combine) {
                 __syncwarp();  // all lanes have read the partial: the slot is free again
-                if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 0);
+                if (lane == 0) {
+                    st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 0);
+                    a.flags[slot * kTcFlagsPerSlot + kTcTicketOffset + ep] = 0;
+                }
             }
         }
         if (lane == 0) dev::bulk_wait_group<0>();

@@ -68,6 +68,25 @@ int conv_bn_silu_fold(const float *gamma, const float *beta, const float *mean, 
                       float eps, int c_out, float *scale, float *bias, void *stream);
 
 /*
+ * The same fold for several layers in one launch (a network's layers at load
+ * time, or every layer of a step): layer i's arguments and results are those
+ * of conv_bn_silu_fold with layers[i]'s fields; the results are bit-identical.
+ *   layers   : host array of n_layers descriptors, read during the call only
+ *   n_layers : >= 0; 0 is a no-op.  Layers with c_out == 0 are skipped.
+ * Every layer is validated before anything is launched (the first invalid
+ * one decides the status).  Output arrays of different layers must not
+ * overlap each other or any input.
+ */
+typedef struct cbs_fold_layer {
+    const float *gamma, *beta, *mean, *var; /* device, float32 [c_out] */
+    float eps;                              /* >= 0 and finite */
+    int c_out;
+    float *scale, *bias;                    /* device, float32 [c_out], written */
+} cbs_fold_layer;
+
+int conv_bn_silu_fold_batch(const cbs_fold_layer *layers, int n_layers, void *stream);
+
+/*
  * Fused forward pass: y = SiLU(conv2d(x, W) * scale + bias).
  * ("Fusing an Epilogue", section "The shape of it": the K loop accumulates
  * the output tile, then acc = acc*bn_scale + bn_bias, acc = acc*sigmoid(acc),

@@ -146,6 +146,20 @@ def test_invalid_arguments_return_status_without_gpu(lib):
     assert silu_apply(good, None, 8, None) == lib.CBS_ERR_INVALID_ARG
     assert silu_apply(odd, good, 8, None) == lib.CBS_ERR_MISALIGNED
     assert silu_apply(None, None, 0, None) == lib.CBS_OK
+    # batched fold: every layer validated before any launch
+    FL = lib.FoldLayer
+    ok_layer = FL(0x10000, 0x10000, 0x10000, 0x10000, 1e-3, 4, 0x10000, 0x10000)
+    fb = lib._lib.conv_bn_silu_fold_batch
+    arr = (FL * 2)(ok_layer, FL(0x10000, None, 0x10000, 0x10000, 1e-3, 4, 0x10000, 0x10000))
+    assert fb(arr, 2, None) == lib.CBS_ERR_INVALID_ARG
+    arr = (FL * 2)(ok_layer, FL(0x10000, 0x10008, 0x10000, 0x10000, 1e-3, 4, 0x10000, 0x10000))
+    assert fb(arr, 2, None) == lib.CBS_ERR_MISALIGNED
+    arr = (FL * 1)(FL(0x10000, 0x10000, 0x10000, 0x10000, -1.0, 4, 0x10000, 0x10000))
+    assert fb(arr, 1, None) == lib.CBS_ERR_INVALID_ARG
+    assert fb(None, -1, None) == lib.CBS_ERR_INVALID_ARG
+    assert fb(None, 0, None) == lib.CBS_OK
+    arr = (FL * 1)(FL(None, None, None, None, 1e-3, 0, None, None))
+    assert fb(arr, 1, None) == lib.CBS_OK                  # c_out == 0 layers are skipped
     # fold: negative eps, null pointers, misaligned, c_out == 0
     fold = lib._lib.conv_bn_silu_fold
     assert fold(good, good, good, good, -1.0, 4, good, good, None) == lib.CBS_ERR_INVALID_ARG

@@ -87,6 +87,23 @@ def test_fold_matches_oracle(capi):
         assert np.all(np.abs(gb - ref_b) <= 2 * np.spacing(np.abs(ref_b).astype(np.float32))), name
 
 
+def test_fold_batch_is_bit_identical_to_single_folds(capi):
+    """One batched launch over the five layers (plus an empty one) gives exactly the
+    scale/bias of the per-layer fold."""
+    layers, singles = [], []
+    for name in LAYER_ORDER:
+        inp = make_layer_inputs(LAYERS[name])
+        _, _, (g, b, m, v) = to_dev(inp)
+        s1, b1 = capi.fold(g, b, m, v, inp.eps)
+        singles.append((s1, b1))
+        layers.append((g, b, m, v, inp.eps, torch.full_like(s1, float("nan")), torch.full_like(b1, float("nan"))))
+    empty = torch.empty(0, dtype=torch.float32, device="cuda:0")
+    capi.fold_batch(layers[:2] + [(empty, empty, empty, empty, 1e-3, empty, empty)] + layers[2:])
+    torch.cuda.synchronize()
+    for (s1, b1), lay in zip(singles, layers):
+        assert torch.equal(s1, lay[5]) and torch.equal(b1, lay[6])
+
+
 # ------------------------------------------------------------------ the five layers, full size
 @pytest.mark.parametrize("name", LAYER_ORDER)
 def test_layer_full_size_default_kernel(capi, name):
