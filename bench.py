@@ -79,6 +79,8 @@ def parse_args(argv=None):
                     help="calls per layer for the per-layer (L2-flushed) timings")
     ap.add_argument("--no-unfused", action="store_true",
                     help="skip the fused-vs-unfused comparison (conv, BN and SiLU as three kernels)")
+    ap.add_argument("--no-epilogues", action="store_true",
+                    help="skip the per-layer timing of the other epilogues (identity, ReLU, residual add)")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch through the API each step instead of replaying CUDA graphs")
     args = ap.parse_args(argv)
@@ -391,6 +393,9 @@ def run_ours(args, rank, world, local_rank):
     fusion = None if args.no_unfused else \
         fusion_comparison(capi, sets, layers, stream, dev, args.iso_iters, iso)
 
+    epilogues = None if args.no_epilogues else \
+        epilogue_variants(capi, sets, layers, stream, dev, args.iso_iters, iso)
+
     e2e = run_e2e(args, capi, inputs, dev, stream, world) if args.e2e_steps > 0 else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -414,6 +419,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "per_layer": per_layer,
         "fusion": fusion,
+        "epilogues": epilogues,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
@@ -488,6 +494,40 @@ def fusion_comparison(capi, sets, layers, stream, dev, iters, fused_us) -> dict:
     return {"layers": out, "fused_us_total": round(tot_f, 3), "unfused_us_total": round(tot_u, 3),
             "speedup_total": round(tot_u / tot_f, 3),
             "timing": "median of isolated calls, L2 flushed before each; unfused = 3 launches"}
+
+
+def epilogue_variants(capi, sets, layers, stream, dev, iters, silu_us) -> dict:
+    """Each layer timed alone (L2 flushed before every call) with the other epilogues of
+    conv_bn_act_forward: BN only, BN + ReLU, and BN + SiLU + a residual add (which reads a
+    second output-sized tensor), next to the fused SiLU layer itself."""
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    out = {}
+    with torch.cuda.stream(stream):
+        for n in layers:
+            sh = LAYERS[n]
+            res = torch.randn((sh.n, sh.ho, sh.wo, sh.k), device=dev).to(torch.bfloat16)
+            row = {"silu_us": round(silu_us[n], 3)}
+            for label, act, r in (("identity_us", "identity", None), ("relu_us", "relu", None),
+                                  ("silu_residual_us", "silu", res)):
+                evs = []
+                for i in range(iters):
+                    lb = sets[i % ROTATION][n]
+                    flush.zero_()
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    capi.forward_act(lb.x, lb.w, lb.scale, lb.bias, sh.stride, sh.pad, activation=act,
+                                     residual=r, y=lb.y, stream=stream)
+                    b.record(stream)
+                    evs.append((a, b))
+                torch.cuda.synchronize()
+                capi.check(stream)
+                row[label] = round(1e3 * statistics.median(a.elapsed_time(b) for a, b in evs), 3)
+            out[n] = row
+            del res
+    del flush
+    return {"layers": out, "timing": "median of isolated calls, L2 flushed before each",
+            "residual_bytes_note": "the residual add reads one more bf16 tensor the size of y"}
 
 
 def run_e2e(args, capi, inputs, dev, stream, world):

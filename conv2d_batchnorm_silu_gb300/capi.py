@@ -31,6 +31,7 @@ CBS_ERR_CUDA = 4
 CBS_ERR_TIMEOUT = 5
 
 ALGOS = {"auto": 0, "tcgen05": 1, "direct": 2}
+ACTIVATIONS = {"silu": 0, "identity": 1, "relu": 2}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 
 _i = ctypes.c_int
@@ -67,6 +68,7 @@ _fold_batch = _declare("conv_bn_silu_fold_batch", [ctypes.POINTER(FoldLayer), _i
 _forward = _declare("conv_bn_silu_forward", [_p] * 5 + [_i] * 11 + [_p])
 _forward_algo = _declare("conv_bn_silu_forward_algo", [_p] * 5 + [_i] * 12 + [_p])
 _forward_noalloc = _declare("conv_bn_silu_forward_noalloc", [_p] * 5 + [_i] * 11 + [_p])
+_forward_act = _declare("conv_bn_act_forward", [_p] * 6 + [_i] * 12 + [_p])
 _forward_unfused = _declare("conv_bn_silu_forward_unfused", [_p] * 7 + [_i] * 11 + [_p])
 _bn_apply = _declare("conv_bn_silu_bn_apply", [_p] * 4 + [ctypes.c_longlong, _i, _p])
 _silu_apply = _declare("conv_bn_silu_silu_apply", [_p, _p, ctypes.c_longlong, _p])
@@ -223,6 +225,44 @@ def forward(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor, bias: torch.T
     st = _forward_algo(px, pw_, ps, pb, py, n, h, wi, c, c_out, r, s, sh, sw, ph, pw,
                        ALGOS[algo], _stream_handle(stream))
     _raise_if(st, "conv_bn_silu_forward")
+    return y
+
+
+def forward_act(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor, bias: torch.Tensor,
+                stride=1, pad=0, activation: str = "silu", residual: torch.Tensor | None = None,
+                y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """conv_bn_act_forward: y = act(conv2d(x, w) * scale + bias) [+ residual].
+
+    activation: "silu", "identity" or "relu"; residual: bf16 NHWC like y (may be y itself).
+    """
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(ACTIVATIONS)}")
+    if x.dim() != 4 or w.dim() != 4:
+        raise ValueError("x must be NHWC and w KRSC (4-D)")
+    n, h, wi, c = x.shape
+    c_out, r, s, c2 = w.shape
+    if c2 != c:
+        raise ValueError(f"channel mismatch: x has {c}, w has {c2}")
+    if scale.numel() != c_out or bias.numel() != c_out:
+        raise ValueError("scale and bias must have c_out elements")
+    sh, sw = _pair(stride)
+    ph, pw = _pair(pad)
+    ho, wo = output_dims(h, wi, r, s, (sh, sw), (ph, pw))
+    shape = (n, ho, wo, c_out)
+    if y is None:
+        y = torch.empty(shape, dtype=torch.bfloat16, device=x.device)
+    elif tuple(y.shape) != shape:
+        raise ValueError(f"y has shape {tuple(y.shape)}, expected {shape}")
+    if residual is not None and tuple(residual.shape) != shape:
+        raise ValueError(f"residual has shape {tuple(residual.shape)}, expected {shape}")
+    if y.numel() == 0:
+        return y
+    pres = _dev_tensor(residual, torch.bfloat16, "residual") if residual is not None else None
+    st = _forward_act(_dev_tensor(x, torch.bfloat16, "x"), _dev_tensor(w, torch.bfloat16, "w"),
+                      _dev_tensor(scale, torch.float32, "scale"), _dev_tensor(bias, torch.float32, "bias"),
+                      pres, _dev_tensor(y, torch.bfloat16, "y"), n, h, wi, c, c_out, r, s, sh, sw, ph, pw,
+                      ACTIVATIONS[activation], _stream_handle(stream))
+    _raise_if(st, "conv_bn_act_forward")
     return y
 
 

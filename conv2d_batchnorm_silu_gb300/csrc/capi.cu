@@ -248,6 +248,36 @@ int conv_bn_silu_forward_algo(const void *x, const void *w, const float *scale, 
     return launch_forward(p, algo, static_cast<cudaStream_t>(stream));
 }
 
+int conv_bn_act_forward(const void *x, const void *w, const float *scale, const float *bias,
+                        const void *residual, void *y, int n, int h, int w_in, int c, int c_out, int r,
+                        int s, int stride_h, int stride_w, int pad_h, int pad_w, int activation,
+                        void *stream)
+{
+    int mode;
+    switch (activation) {
+    case CBS_ACT_SILU: mode = cbs::kEpiSilu; break;
+    case CBS_ACT_IDENTITY: mode = cbs::kEpiBn; break;
+    case CBS_ACT_RELU: mode = cbs::kEpiRelu; break;
+    default: return CBS_ERR_INVALID_ARG;
+    }
+    cbs::ConvProblem p{};
+    int st = make_problem(n, h, w_in, c, c_out, r, s, stride_h, stride_w, pad_h, pad_w, &p);
+    if (st != CBS_OK) return st;
+    if (p.m == 0 || c_out == 0) return CBS_OK;
+    if (!x || !w || !scale || !bias || !y) return CBS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(scale) || !aligned16(bias) || !aligned16(y) ||
+        (residual && !aligned16(residual)))
+        return CBS_ERR_MISALIGNED;
+    p.x = x;
+    p.w = w;
+    p.scale = scale;
+    p.bias = bias;
+    p.y = y;
+    p.epi_mode = mode;
+    p.residual = residual;
+    return launch_forward(p, CBS_ALGO_AUTO, static_cast<cudaStream_t>(stream));
+}
+
 int conv_bn_silu_forward_unfused(const void *x, const void *w, const float *scale, const float *bias,
                                  void *t1, void *t2, void *y, int n, int h, int w_in, int c, int c_out,
                                  int r, int s, int stride_h, int stride_w, int pad_h, int pad_w,
@@ -266,7 +296,7 @@ int conv_bn_silu_forward_unfused(const void *x, const void *w, const float *scal
     p.scale = scale;
     p.bias = bias;
     p.y = t1;
-    p.conv_only = 1;
+    p.epi_mode = cbs::kEpiConvOnly;
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     st = launch_forward(p, CBS_ALGO_AUTO, strm);
     if (st != CBS_OK) return st;

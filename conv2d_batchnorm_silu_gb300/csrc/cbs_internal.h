@@ -7,6 +7,15 @@
 
 namespace cbs {
 
+// What the epilogue applies to the accumulator (a kernel argument, uniform
+// over the launch).
+enum EpiMode : int {
+    kEpiSilu = 0,      // SiLU(acc*scale + bias): the fused layer
+    kEpiConvOnly = 1,  // acc: the unfused comparator's first step stores t1 = conv(x, W)
+    kEpiBn = 2,        // acc*scale + bias: BN (or a plain per-channel bias) without activation
+    kEpiRelu = 3,      // max(acc*scale + bias, 0)
+};
+
 // One convolution call, with the derived GEMM view M = n*ho*wo, N = c_out, K = c*r*s.
 struct ConvProblem {
     const void *x;
@@ -18,7 +27,8 @@ struct ConvProblem {
     int stride_h, stride_w, pad_h, pad_w;
     int ho, wo;
     long long m;    // output pixels
-    int conv_only;  // 1: store the bf16 convolution only (no BN, no SiLU) -- unfused comparator
+    int epi_mode;          // EpiMode: SiLU (the layer), conv only, BN only, BN + ReLU
+    const void *residual;  // nullable bf16 NHWC [m][c_out], added after the activation
 };
 
 // Tile configuration of the tcgen05 implicit GEMM.

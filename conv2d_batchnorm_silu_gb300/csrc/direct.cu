@@ -32,8 +32,42 @@ struct DirectArgs {
     long long m;
     int h, w_in, c, c_out, r, s;
     int stride_h, stride_w, pad_h, pad_w, ho, wo;
-    int conv_only;  // 1: store the raw convolution (unfused comparator)
+    int epi_mode;   // EpiMode applied to the accumulator
+    const __nv_bfloat16 *residual;  // nullable: bf16 [m][c_out] added after the activation
 };
+
+// Epilogue on the registers: BN multiply/add, activation, optional residual,
+// bf16, 16-byte stores when the channel run allows.
+__device__ __forceinline__ void store_outputs(const DirectArgs &a, long long m, int k0, const float *acc)
+{
+    __nv_bfloat16 *yp = a.y + m * a.c_out + k0;
+    const __nv_bfloat16 *rp = a.residual != nullptr ? a.residual + m * a.c_out + k0 : nullptr;
+    if (k0 + KB <= a.c_out && (a.c_out % 8) == 0) {
+        float f[KB];
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+            f[j] = dev::epilogue_value(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j), a.epi_mode);
+        if (rp != nullptr) {
+#pragma unroll
+            for (int j = 0; j < KB; j += 8) dev::add_residual8(f + j, rp + j);
+        }
+        uint32_t packed[KB / 2];
+#pragma unroll
+        for (int j = 0; j < KB; j += 2) packed[j / 2] = dev::pack_bf16x2(f[j], f[j + 1]);
+        uint4 *dst = reinterpret_cast<uint4 *>(yp);
+#pragma unroll
+        for (int v = 0; v < KB / 8; ++v)
+            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+            if (k0 + j < a.c_out) {
+                float f = dev::epilogue_value(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j), a.epi_mode);
+                if (rp != nullptr) f += __bfloat162float(rp[j]);
+                yp[j] = __float2bfloat16_rn(f);
+            }
+    }
+}
 
 __global__ void __launch_bounds__(kDirectThreads)
     direct_conv_bn_silu_kernel(const DirectArgs a)
@@ -97,25 +131,7 @@ __global__ void __launch_bounds__(kDirectThreads)
         }
     }
     if (!active) return;
-    // Epilogue on the registers: BN multiply/add, SiLU, bf16, one store per channel pair.
-    __nv_bfloat16 *yp = a.y + m * a.c_out + k0;
-    if (k0 + KB <= a.c_out && (a.c_out % 8) == 0) {
-        uint32_t packed[KB / 2];
-#pragma unroll
-        for (int j = 0; j < KB; j += 2)
-            packed[j / 2] = dev::pack_bf16x2(dev::epilogue_value(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j), a.conv_only),
-                                             dev::epilogue_value(acc[j + 1], __ldg(a.scale + k0 + j + 1),
-                                                                 __ldg(a.bias + k0 + j + 1), a.conv_only));
-        uint4 *dst = reinterpret_cast<uint4 *>(yp);
-#pragma unroll
-        for (int v = 0; v < KB / 8; ++v)
-            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < KB; ++j)
-            if (k0 + j < a.c_out)
-                yp[j] = __float2bfloat16_rn(dev::epilogue_value(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j), a.conv_only));
-    }
+    store_outputs(a, m, k0, acc);
 }
 
 // Small filters with a compile-time shape (R x S taps of C channels): every
@@ -195,24 +211,7 @@ __global__ void __launch_bounds__(NT) direct_small_kernel(const DirectArgs a)
         }
     }
     if (!active) return;
-    __nv_bfloat16 *yp = a.y + m * a.c_out + k0;
-    if (k0 + KB <= a.c_out && (a.c_out % 8) == 0) {
-        uint32_t packed[KB / 2];
-#pragma unroll
-        for (int j = 0; j < KB; j += 2)
-            packed[j / 2] = dev::pack_bf16x2(dev::epilogue_value(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j), a.conv_only),
-                                             dev::epilogue_value(acc[j + 1], __ldg(a.scale + k0 + j + 1),
-                                                                 __ldg(a.bias + k0 + j + 1), a.conv_only));
-        uint4 *dst = reinterpret_cast<uint4 *>(yp);
-#pragma unroll
-        for (int v = 0; v < KB / 8; ++v)
-            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < KB; ++j)
-            if (k0 + j < a.c_out)
-                yp[j] = __float2bfloat16_rn(dev::epilogue_value(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j), a.conv_only));
-    }
+    store_outputs(a, m, k0, acc);
 }
 
 constexpr int kSmallThreads = 64;
@@ -258,7 +257,8 @@ cudaError_t direct_launch(const ConvProblem &p, cudaStream_t stream)
     a.pad_w = p.pad_w;
     a.ho = p.ho;
     a.wo = p.wo;
-    a.conv_only = p.conv_only;
+    a.epi_mode = p.epi_mode;
+    a.residual = static_cast<const __nv_bfloat16 *>(p.residual);
     cudaError_t err = cudaSuccess;
     if (try_small<3, 3, 1>(p, a, stream, &err) || try_small<3, 3, 3>(p, a, stream, &err) ||
         try_small<3, 3, 4>(p, a, stream, &err) || try_small<3, 3, 8>(p, a, stream, &err) ||

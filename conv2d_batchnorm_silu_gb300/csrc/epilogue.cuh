@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "cbs_internal.h"
+
 namespace cbs {
 namespace dev {
 
@@ -36,12 +38,40 @@ __device__ __forceinline__ float bn_silu(float acc, float scale, float bias)
     return silu_from_half(fmaf(acc, 0.5f * scale, 0.5f * bias));
 }
 
-// The fused epilogue, or (conv_only) the raw convolution output: the unfused
-// comparator's first step stores t1 = conv(x, W) and leaves BN and SiLU to
-// separate kernels.
-__device__ __forceinline__ float epilogue_value(float acc, float scale, float bias, int conv_only)
+__device__ __forceinline__ float epilogue_value(float acc, float scale, float bias, int mode)
 {
-    return conv_only ? acc : bn_silu(acc, scale, bias);
+    if (mode == kEpiSilu) return bn_silu(acc, scale, bias);
+    if (mode == kEpiConvOnly) return acc;
+    const float z = fmaf(acc, scale, bias);
+    return mode == kEpiRelu ? fmaxf(z, 0.0f) : z;
+}
+
+// SiLU from precomputed halves (h = acc*scale/2 + bias/2), or the other modes
+// from the same halves: z = 2h exactly (a power-of-two scaling).
+__device__ __forceinline__ float epilogue_from_half(float acc, float half_scale, float half_bias, int mode)
+{
+    if (mode == kEpiConvOnly) return acc;
+    const float h = fmaf(acc, half_scale, half_bias);
+    if (mode == kEpiSilu) return silu_from_half(h);
+    const float z = 2.0f * h;
+    return mode == kEpiRelu ? fmaxf(z, 0.0f) : z;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// Eight consecutive bf16 values of a residual tensor (16-byte aligned), added
+// to v[0..7] after the activation.
+__device__ __forceinline__ void add_residual8(float *v, const void *src)
+{
+    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(src));
+    v[0] += __uint_as_float(r.x << 16);
+    v[1] += __uint_as_float(r.x & 0xffff0000u);
+    v[2] += __uint_as_float(r.y << 16);
+    v[3] += __uint_as_float(r.y & 0xffff0000u);
+    v[4] += __uint_as_float(r.z << 16);
+    v[5] += __uint_as_float(r.z & 0xffff0000u);
+    v[6] += __uint_as_float(r.w << 16);
+    v[7] += __uint_as_float(r.w & 0xffff0000u);
 }
 
 // Two floats -> packed bf16x2 (round to nearest even), `lo` in the low half,

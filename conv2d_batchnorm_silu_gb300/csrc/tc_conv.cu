@@ -52,7 +52,8 @@ struct TcArgs {
     int stride_h, stride_w, pad_h, pad_w;
     int s;
     int c_chunks, k_iters;
-    int conv_only;   // 1: store the raw convolution (unfused comparator)
+    int epi_mode;    // EpiMode applied to the accumulator
+    const __nv_bfloat16 *residual;  // nullable: bf16 [m][c_out] added after the activation
     int stream_k;    // 1: each CTA takes an equal share of all K steps (see WorkIter)
     float *partial;  // stream-K: [grid-1][128*BN] fp32 partial tiles (slot c: boundary of CTAs c, c+1)
     int *flags;      // stream-K: per slot, a ready flag and an arrival ticket per epilogue warp; 0 between launches
@@ -228,13 +229,29 @@ __device__ __forceinline__ uint32_t swizzle_offset(uint32_t off)
 // them.  Both CTAs' loads complete on the even CTA's full barrier; its MMA
 // commits release the stage, and publish a finished accumulator, in both CTAs;
 // both CTAs' epilogue warps hand the accumulator back to the even CTA.
-template <int BN, int BK, bool SWAP, bool PAIR>
+// EPI: which epilogue the instantiation carries, so that the fused layer's own
+// (BN + SiLU) pays nothing for the others -- kEpiKindSilu, kEpiKindMode (the
+// launch's EpiMode, chosen at run time) or kEpiKindResidual (the same, plus a
+// residual tensor added after the activation).
+constexpr int kEpiKindSilu = 0;
+constexpr int kEpiKindMode = 1;
+constexpr int kEpiKindResidual = 2;
+
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+template <int BN, int BK, bool SWAP, bool PAIR, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_conv_bn_silu_kernel(const __grid_constant__ CUtensorMap tm_x,
                            const __grid_constant__ CUtensorMap tm_w,
                            const __grid_constant__ CUtensorMap tm_y, const TcArgs a)
 {
     static_assert(!(SWAP && PAIR), "CTA pairs serve the pixel-major (unswapped) tile only");
+    constexpr bool RES = EPI == kEpiKindResidual;
+    // The epilogue mode: a compile-time constant for the fused layer.
+    const int emode = EPI == kEpiKindSilu ? (int)kEpiSilu : a.epi_mode;
     constexpr int CG = PAIR ? 2 : 1;  // tcgen05 CTA group
     using C = TcCfg<BN, BK, PAIR ? BN / 2 : BN>;
     constexpr int STAGES = C::STAGES;
@@ -464,6 +481,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int row = ew * 32 + lane;  // this thread's row of the tile (TMEM lane)
         WorkIter wi(a, vb, vg);
         WorkUnit u;
+        // Residual epilogue: bring a unit's residual rows (this warp's part) into L2
+        // while its K loop runs, so that the epilogue's loads of them hit L2.
+        auto prefetch_residual = [&](const WorkUnit &q) {
+            if constexpr (RES) {
+                if constexpr (SWAP) {
+                    const int pt = q.tile / a.n_tiles;
+                    const int chw = (q.tile - pt * a.n_tiles) * C::BM + ew * 32;
+                    if (chw < a.c_out) {
+                        for (int i = 0; i < C::EPI_COLS / 32; ++i) {
+                            const int px = pt * BN + col_base + i * 32 + lane;
+                            if (px < a.m) prefetch_l2(a.residual + (size_t)px * a.c_out + chw);
+                        }
+                    }
+                } else {
+                    const int mu = q.tile / a.n_tiles;
+                    const int mt = PAIR ? 2 * mu + rank : mu;
+                    const int c0 = (q.tile - mu * a.n_tiles) * BN + col_base;
+                    const int px = mt * C::BM + ew * 32 + lane;
+                    if (px < a.m && c0 < a.c_out) {
+                        const int bytes = 2 * (a.c_out - c0 < C::EPI_COLS ? a.c_out - c0 : C::EPI_COLS);
+                        const char *rp = reinterpret_cast<const char *>(a.residual + (size_t)px * a.c_out + c0);
+                        for (int b = 0; b < bytes; b += 128) prefetch_l2(rp + b);
+                    }
+                }
+            }
+        };
+        if constexpr (RES) {
+            WorkIter first = wi;
+            WorkUnit q;
+            if (first.next(a, q)) prefetch_residual(q);
+        }
         for (; wi.next(a, u); ++lt) {
             const int buf = lt & 1;
             const uint32_t tparity = (uint32_t)(lt >> 1) & 1u;
@@ -479,6 +527,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             dev::tc_fence_after_sync();
+            if constexpr (RES) {
+                WorkIter after = wi;  // already past u
+                WorkUnit q;
+                if (after.next(a, q)) prefetch_residual(q);
+            }
             if constexpr (SWAP) {
                 // TMEM lane = output channel, column = pixel.  Each thread owns one
                 // channel, so BN scale/bias are per-thread constants; the tile is
@@ -509,14 +562,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) dev::bulk_wait_group_read<1>();
                     __syncwarp();
                     __nv_bfloat16 *sb = reinterpret_cast<__nv_bfloat16 *>(my_stg + sbuf * C::STG_BYTES);
+                    const int px0 = px_base + j * EC;
+                    if constexpr (RES) {
+                        // Residual of this lane's channel for the chunk's pixels (across the
+                        // warp, one 64-byte run of channels per pixel), all loaded first.
+                        float rv[EC];
 #pragma unroll
-                    for (int pp = 0; pp < EC; ++pp)  // row pp: 32 channels, one per lane
-                        sb[pp * 32 + lane] =
-                            __float2bfloat16_rn(a.conv_only ? __uint_as_float(v[pp])
-                                                            : dev::silu_from_half(fmaf(__uint_as_float(v[pp]), hs, hb)));
+                        for (int pp = 0; pp < EC; ++pp)
+                            rv[pp] = (ch < a.c_out && px0 + pp < a.m)
+                                         ? __bfloat162float(__ldg(a.residual + (size_t)(px0 + pp) * a.c_out + ch))
+                                         : 0.f;
+#pragma unroll
+                        for (int pp = 0; pp < EC; ++pp)
+                            sb[pp * 32 + lane] = __float2bfloat16_rn(
+                                dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, emode) + rv[pp]);
+                    } else {
+#pragma unroll
+                        for (int pp = 0; pp < EC; ++pp)  // row pp: 32 channels, one per lane
+                            sb[pp * 32 + lane] = __float2bfloat16_rn(
+                                dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, emode));
+                    }
                     dev::fence_proxy_async_shared();
                     __syncwarp();
-                    const int px0 = px_base + j * EC;
                     if (lane == 0 && px0 < a.m && ch_w0 < a.c_out) {
                         dev::tma_store_2d(&tm_y, dev::smem_u32(sb), ch_w0, px0);
                         dev::bulk_commit_group();
@@ -602,17 +669,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 const int ch0 = n0 + col_base + j * EC;
                 uint32_t packed[EC / 2];
-                if (ch0 + EC <= a.c_out) {
+                if constexpr (RES) {
+                    // With a residual: this lane's pixel row, channels ch0.. (8 per 16-byte
+                    // load; c_out % 8 == 0, so a group of 8 is wholly inside or outside).
+                    const int pix = row0 + lane;
+                    uint4 rr[EC / 8];
+#pragma unroll
+                    for (int g = 0; g < EC / 8; ++g)
+                        rr[g] = (pix < a.m && ch0 + 8 * g < a.c_out)
+                                    ? __ldg(reinterpret_cast<const uint4 *>(a.residual + (size_t)pix * a.c_out + ch0 +
+                                                                            8 * g))
+                                    : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int i = 0; i < EC; i += 8) {
+                        const uint32_t rw[4] = {rr[i / 8].x, rr[i / 8].y, rr[i / 8].z, rr[i / 8].w};
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            const int c = ch0 + i + e;
+                            const float f0 = c < a.c_out ? dev::epilogue_value(__uint_as_float(v[i + e]), __ldg(a.scale + c),
+                                                                               __ldg(a.bias + c), emode)
+                                                         : 0.f;
+                            const float f1 = c + 1 < a.c_out
+                                                 ? dev::epilogue_value(__uint_as_float(v[i + e + 1]), __ldg(a.scale + c + 1),
+                                                                       __ldg(a.bias + c + 1), emode)
+                                                 : 0.f;
+                            packed[(i + e) / 2] = dev::pack_bf16x2(f0 + __uint_as_float(rw[e / 2] << 16),
+                                                                   f1 + __uint_as_float(rw[e / 2] & 0xffff0000u));
+                        }
+                    }
+                } else if (ch0 + EC <= a.c_out) {
 #pragma unroll
                     for (int i = 0; i < EC; i += 4) {
                         const float4 sc = __ldg(reinterpret_cast<const float4 *>(a.scale + ch0 + i));
                         const float4 bi = __ldg(reinterpret_cast<const float4 *>(a.bias + ch0 + i));
                         packed[i / 2] = dev::pack_bf16x2(
-                            dev::epilogue_value(__uint_as_float(v[i]), sc.x, bi.x, a.conv_only),
-                            dev::epilogue_value(__uint_as_float(v[i + 1]), sc.y, bi.y, a.conv_only));
+                            dev::epilogue_value(__uint_as_float(v[i]), sc.x, bi.x, emode),
+                            dev::epilogue_value(__uint_as_float(v[i + 1]), sc.y, bi.y, emode));
                         packed[i / 2 + 1] =
-                            dev::pack_bf16x2(dev::epilogue_value(__uint_as_float(v[i + 2]), sc.z, bi.z, a.conv_only),
-                                             dev::epilogue_value(__uint_as_float(v[i + 3]), sc.w, bi.w, a.conv_only));
+                            dev::pack_bf16x2(dev::epilogue_value(__uint_as_float(v[i + 2]), sc.z, bi.z, emode),
+                                             dev::epilogue_value(__uint_as_float(v[i + 3]), sc.w, bi.w, emode));
                     }
                 } else {
 #pragma unroll
@@ -622,8 +717,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const float b0 = c0 < a.c_out ? __ldg(a.bias + c0) : 0.f;
                         const float s1 = c1 < a.c_out ? __ldg(a.scale + c1) : 0.f;
                         const float b1 = c1 < a.c_out ? __ldg(a.bias + c1) : 0.f;
-                        packed[i / 2] = dev::pack_bf16x2(dev::epilogue_value(__uint_as_float(v[i]), s0, b0, a.conv_only),
-                                                         dev::epilogue_value(__uint_as_float(v[i + 1]), s1, b1, a.conv_only));
+                        packed[i / 2] = dev::pack_bf16x2(dev::epilogue_value(__uint_as_float(v[i]), s0, b0, emode),
+                                                         dev::epilogue_value(__uint_as_float(v[i + 1]), s1, b1, emode));
                     }
                 }
                 // Stage the warp's 32 rows x EC channels, then one TMA store.
@@ -877,12 +972,12 @@ cudaError_t stream_k_workspace(cudaStream_t stream, size_t bytes, size_t flag_by
     return cudaSuccess;
 }
 
-template <int BN, int BK, bool SWAP, bool PAIR>
+template <int BN, int BK, bool SWAP, bool PAIR, int EPI>
 cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &maps, cudaStream_t stream,
                        void *caller_workspace)
 {
     using C = TcCfg<BN, BK, PAIR ? BN / 2 : BN>;
-    auto kern = tc_conv_bn_silu_kernel<BN, BK, SWAP, PAIR>;
+    auto kern = tc_conv_bn_silu_kernel<BN, BK, SWAP, PAIR, EPI>;
     // The shared-memory opt-in is per function and device: done once per device.
     static std::mutex attr_mu;
     static unsigned long long attr_done = 0;  // bit per device ordinal (< 64)
@@ -914,7 +1009,8 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
     a.s = p.s;
     a.c_chunks = plan.c_chunks;
     a.k_iters = plan.k_iters;
-    a.conv_only = p.conv_only;
+    a.epi_mode = p.epi_mode;
+    a.residual = static_cast<const __nv_bfloat16 *>(p.residual);
     a.stream_k = plan.stream_k;
     a.partial = nullptr;
     a.flags = nullptr;
@@ -1059,29 +1155,29 @@ cudaError_t tc_launch(const ConvProblem &p, const TcPlan &plan, cudaStream_t str
     return tc_launch_with_workspace(p, plan, stream, nullptr);
 }
 
-cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream,
-                                     void *workspace)
+namespace {
+
+template <int EPI>
+cudaError_t dispatch(const ConvProblem &p, const TcPlan &plan, const TcMaps &maps, cudaStream_t stream,
+                     void *workspace)
 {
-    TcMaps maps;
-    cudaError_t st = cached_maps(p, plan.block_n, plan.block_k, plan.swap_ab != 0, plan.pair != 0, &maps);
-    if (st != cudaSuccess) return st;
     if (plan.swap_ab) {
         if (plan.block_n != 256) return cudaErrorInvalidConfiguration;
-        if (plan.block_k == 64) return launch_cfg<256, 64, true, false>(p, plan, maps, stream, workspace);
-        if (plan.block_k == 32) return launch_cfg<256, 32, true, false>(p, plan, maps, stream, workspace);
-        if (plan.block_k == 16) return launch_cfg<256, 16, true, false>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 64) return launch_cfg<256, 64, true, false, EPI>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 32) return launch_cfg<256, 32, true, false, EPI>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 16) return launch_cfg<256, 16, true, false, EPI>(p, plan, maps, stream, workspace);
         return cudaErrorInvalidConfiguration;
     }
     if (plan.pair) {
         if (plan.block_n != 256) return cudaErrorInvalidConfiguration;
-        if (plan.block_k == 64) return launch_cfg<256, 64, false, true>(p, plan, maps, stream, workspace);
-        if (plan.block_k == 32) return launch_cfg<256, 32, false, true>(p, plan, maps, stream, workspace);
-        if (plan.block_k == 16) return launch_cfg<256, 16, false, true>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 64) return launch_cfg<256, 64, false, true, EPI>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 32) return launch_cfg<256, 32, false, true, EPI>(p, plan, maps, stream, workspace);
+        if (plan.block_k == 16) return launch_cfg<256, 16, false, true, EPI>(p, plan, maps, stream, workspace);
         return cudaErrorInvalidConfiguration;
     }
 #define CBS_TC_CASE(BN_, BK_) \
     if (plan.block_n == BN_ && plan.block_k == BK_)       \
-        return launch_cfg<BN_, BK_, false, false>(p, plan, maps, stream, workspace);
+        return launch_cfg<BN_, BK_, false, false, EPI>(p, plan, maps, stream, workspace);
     CBS_TC_CASE(16, 16) CBS_TC_CASE(16, 32) CBS_TC_CASE(16, 64)
     CBS_TC_CASE(32, 16) CBS_TC_CASE(32, 32) CBS_TC_CASE(32, 64)
     CBS_TC_CASE(64, 16) CBS_TC_CASE(64, 32) CBS_TC_CASE(64, 64)
@@ -1089,6 +1185,19 @@ cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, c
     CBS_TC_CASE(256, 16) CBS_TC_CASE(256, 32) CBS_TC_CASE(256, 64)
 #undef CBS_TC_CASE
     return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace
+
+cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream,
+                                     void *workspace)
+{
+    TcMaps maps;
+    cudaError_t st = cached_maps(p, plan.block_n, plan.block_k, plan.swap_ab != 0, plan.pair != 0, &maps);
+    if (st != cudaSuccess) return st;
+    if (p.residual != nullptr) return dispatch<kEpiKindResidual>(p, plan, maps, stream, workspace);
+    if (p.epi_mode != kEpiSilu) return dispatch<kEpiKindMode>(p, plan, maps, stream, workspace);
+    return dispatch<kEpiKindSilu>(p, plan, maps, stream, workspace);
 }
 
 cudaError_t tc_reset_workspaces()

@@ -48,7 +48,8 @@ struct GatherArgs {
     int m, tiles;
     int h, w_in, c_out, ho, wo, howo;
     int stride_h, stride_w, pad_h, pad_w;
-    int conv_only;  // 1: store the raw convolution (unfused comparator)
+    int epi_mode;   // EpiMode applied to the accumulator
+    const __nv_bfloat16 *residual;  // nullable: bf16 [m][c_out] added after the activation
 };
 
 template <int R, int S, int C, int N>
@@ -296,15 +297,25 @@ __global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kern
             const int m = t * 128 + warp * 32 + lane;
             if (m < a.m) {
                 uint32_t packed[N / 2];
+                if (a.residual != nullptr) {
+                    const __nv_bfloat16 *rp = a.residual + (size_t)m * a.c_out;
 #pragma unroll
-                for (int j = 0; j < N; j += 2)
-                    packed[j / 2] =
-                        a.conv_only
-                            ? dev::pack_bf16x2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]))
-                            : dev::pack_bf16x2(
-                                  dev::silu_from_half(fmaf(__uint_as_float(v[j]), half_scale(j), half_bias(j))),
-                                  dev::silu_from_half(
-                                      fmaf(__uint_as_float(v[j + 1]), half_scale(j + 1), half_bias(j + 1))));
+                    for (int j = 0; j < N; j += 2) {
+                        const float r0 = j < a.c_out ? __bfloat162float(rp[j]) : 0.f;
+                        const float r1 = j + 1 < a.c_out ? __bfloat162float(rp[j + 1]) : 0.f;
+                        packed[j / 2] = dev::pack_bf16x2(
+                            dev::epilogue_from_half(__uint_as_float(v[j]), half_scale(j), half_bias(j), a.epi_mode) + r0,
+                            dev::epilogue_from_half(__uint_as_float(v[j + 1]), half_scale(j + 1), half_bias(j + 1),
+                                                    a.epi_mode) + r1);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < N; j += 2)
+                        packed[j / 2] = dev::pack_bf16x2(
+                            dev::epilogue_from_half(__uint_as_float(v[j]), half_scale(j), half_bias(j), a.epi_mode),
+                            dev::epilogue_from_half(__uint_as_float(v[j + 1]), half_scale(j + 1), half_bias(j + 1),
+                                                    a.epi_mode));
+                }
                 __nv_bfloat16 *yp = a.y + (size_t)m * a.c_out;
                 if (a.c_out == N) {
                     uint4 *dst = reinterpret_cast<uint4 *>(yp);
@@ -366,7 +377,8 @@ bool try_gather(const ConvProblem &p, int sm_count, cudaStream_t stream, cudaErr
     a.stride_w = p.stride_w;
     a.pad_h = p.pad_h;
     a.pad_w = p.pad_w;
-    a.conv_only = p.conv_only;
+    a.epi_mode = p.epi_mode;
+    a.residual = static_cast<const __nv_bfloat16 *>(p.residual);
     const int grid = a.tiles < 2 * sm_count ? a.tiles : 2 * sm_count;
     *err = launch_overlapped(kern, dim3((unsigned)grid), dim3(kGatherThreads), (size_t)G::SMEM, stream, 1, a);
     return true;

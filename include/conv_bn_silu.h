@@ -138,6 +138,34 @@ int conv_bn_silu_forward_noalloc(const void *x, const void *w, const float *scal
                                  void *y, int n, int h, int w_in, int c, int c_out, int r, int s,
                                  int stride_h, int stride_w, int pad_h, int pad_w, void *stream);
 
+/* Activation applied by conv_bn_act_forward after the BN multiply/add. */
+typedef enum cbs_activation {
+    CBS_ACT_SILU = 0,     /* z * sigmoid(z): the layer of conv_bn_silu_forward */
+    CBS_ACT_IDENTITY = 1, /* z: BN (or a plain per-channel bias add) without activation */
+    CBS_ACT_RELU = 2      /* max(z, 0) */
+} cbs_activation;
+
+/*
+ * The fused layer with another epilogue.  "Fusing an Epilogue", section "What
+ * an epilogue is": work that touches each output element once and needs no
+ * neighbours (an activation, a bias add, a scaling) belongs in the epilogue of
+ * the kernel that produced the element; a residual add of a tensor shaped like
+ * y meets the same rule.
+ *   y = act(conv2d(x, W) * scale + bias) [+ residual]
+ * Arguments as conv_bn_silu_forward (the same kernels, chosen the same way), plus
+ *   residual   : device, bf16 NHWC [n][ho][wo][c_out], or NULL for none; added
+ *                after the activation, in fp32, before the one bf16 rounding.
+ *                It may be y itself (an in-place add) but must not otherwise
+ *                overlap y.  16-byte aligned.
+ *   activation : a cbs_activation; anything else returns CBS_ERR_INVALID_ARG.
+ * A plain per-channel bias (no BN) is scale = 1, bias = b with CBS_ACT_IDENTITY.
+ * CBS_ACT_SILU with residual NULL computes exactly what conv_bn_silu_forward does.
+ */
+int conv_bn_act_forward(const void *x, const void *w, const float *scale, const float *bias,
+                        const void *residual, void *y, int n, int h, int w_in, int c, int c_out, int r,
+                        int s, int stride_h, int stride_w, int pad_h, int pad_w, int activation,
+                        void *stream);
+
 /*
  * Unfused comparator: the same layer as the three-kernel sequence that the
  * fusion replaces -- the convolution writes t1 to memory, a BatchNorm kernel

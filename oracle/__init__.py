@@ -1,4 +1,4 @@
-"""Fp64 CPU oracle for y = SiLU(BN(conv2d(x, W))).
+"""Fp64 CPU oracle for y = SiLU(BN(conv2d(x, W))), and its other epilogues.
 
 TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` are the only code allowed to import, call or
@@ -205,3 +205,60 @@ def conv_bn_silu_at(x_bits, w_bits, gamma, beta, mean, var, eps, pixels, stride=
     """The whole layer at selected flat output pixels: float64 [len(pixels), K]."""
     scale, bias = bn_fold(gamma, beta, mean, var, eps)
     return bn_silu(conv2d_at(x_bits, w_bits, pixels, stride, pad, threads), scale, bias)
+
+
+# ---------------------------------------------------------------- other epilogues
+ACTIVATIONS = ("silu", "identity", "relu")
+
+
+def relu(z) -> np.ndarray:
+    """max(z, 0), float64 (an activation the epilogue page names as a candidate)."""
+    z = np.asarray(z, dtype=np.float64)
+    return np.where(z > 0.0, z, 0.0)
+
+
+def activate(z, activation: str) -> np.ndarray:
+    """The activation after the BN multiply/add: "silu" (the layer), "identity" or "relu".
+
+    ("Fusing an Epilogue", section "What an epilogue is": activations and bias
+    adds are element-wise epilogue work.)
+    """
+    if activation == "silu":
+        return silu(z)
+    if activation == "identity":
+        return np.asarray(z, dtype=np.float64)
+    if activation == "relu":
+        return relu(z)
+    raise ValueError(f"unknown activation {activation!r}")
+
+
+def bn_act(conv: np.ndarray, scale, bias, activation: str = "silu", residual=None) -> np.ndarray:
+    """act(acc*scale + bias) [+ residual]: the residual (float64, shaped like the
+    output) is added after the activation, the plainest reading of a residual
+    add placed in the same epilogue."""
+    y = activate(bn(conv, scale, bias), activation)
+    if residual is not None:
+        y = y + np.asarray(residual, dtype=np.float64)
+    return y
+
+
+def conv_bn_act(x_bits, w_bits, gamma, beta, mean, var, eps, stride=1, pad=0, activation: str = "silu",
+                residual_bits=None, threads: int | None = None) -> np.ndarray:
+    """y = act(conv2d(x, W) * scale + bias) [+ residual], float64 NHWC; residual_bits are
+    bf16 bit patterns shaped like the output (decoded exactly)."""
+    scale, bias = bn_fold(gamma, beta, mean, var, eps)
+    res = None if residual_bits is None else bf16_bits_to_f64(residual_bits)
+    return bn_act(conv2d(x_bits, w_bits, stride, pad, threads), scale, bias, activation, res)
+
+
+def conv_bn_act_at(x_bits, w_bits, gamma, beta, mean, var, eps, pixels, stride=1, pad=0,
+                   activation: str = "silu", residual_bits=None, threads: int | None = None) -> np.ndarray:
+    """conv_bn_act at selected flat output pixels: float64 [len(pixels), K]; residual_bits
+    is the full output-shaped residual, from which those pixels' rows are taken."""
+    scale, bias = bn_fold(gamma, beta, mean, var, eps)
+    res = None
+    if residual_bits is not None:
+        k = np.asarray(w_bits).shape[0]
+        res = bf16_bits_to_f64(residual_bits).reshape(-1, k)[np.asarray(pixels)]
+    return bn_act(conv2d_at(x_bits, w_bits, pixels, stride, pad, threads), scale, bias, activation, res)
+

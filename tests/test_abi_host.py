@@ -146,6 +146,14 @@ def test_invalid_arguments_return_status_without_gpu(lib):
     assert silu_apply(good, None, 8, None) == lib.CBS_ERR_INVALID_ARG
     assert silu_apply(odd, good, 8, None) == lib.CBS_ERR_MISALIGNED
     assert silu_apply(None, None, 0, None) == lib.CBS_OK
+    # other epilogues: bad activation id, misaligned residual
+    act = "conv_bn_act_forward"
+    assert f(act, good, good, good, good, None, good, *dims, 7, None) == lib.CBS_ERR_INVALID_ARG
+    assert f(act, good, good, good, good, None, good, *dims, -1, None) == lib.CBS_ERR_INVALID_ARG
+    assert f(act, good, good, good, good, odd, good, *dims, 2, None) == lib.CBS_ERR_MISALIGNED
+    assert f(act, good, good, good, good, good, None, *dims, 1, None) == lib.CBS_ERR_INVALID_ARG
+    assert f(act, None, None, None, None, None, None, 0, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1, 0,
+             None) == lib.CBS_OK
     # batched fold: every layer validated before any launch
     FL = lib.FoldLayer
     ok_layer = FL(0x10000, 0x10000, 0x10000, 0x10000, 1e-3, 4, 0x10000, 0x10000)

@@ -46,6 +46,13 @@ PY_MUTANTS = {
     "plain_sigmoid": ("return z / (1.0 + np.exp(-z))", "return 1.0 / (1.0 + np.exp(-z))"),
     "bias_before_scale": ("return np.asarray(conv, dtype=np.float64) * np.asarray(scale, np.float64) \\\n        + np.asarray(bias, np.float64)",
                           "return (np.asarray(conv, dtype=np.float64) + np.asarray(bias, np.float64)) \\\n        * np.asarray(scale, np.float64)"),
+    "relu_as_abs": ("return np.where(z > 0.0, z, 0.0)", "return np.abs(z)"),
+    "identity_is_silu": ('if activation == "identity":\n        return np.asarray(z, dtype=np.float64)',
+                         'if activation == "identity":\n        return silu(z)'),
+    "residual_before_act": ("y = activate(bn(conv, scale, bias), activation)\n    if residual is not None:\n"
+                            "        y = y + np.asarray(residual, dtype=np.float64)",
+                            "z = bn(conv, scale, bias)\n    if residual is not None:\n"
+                            "        z = z + np.asarray(residual, dtype=np.float64)\n    y = activate(z, activation)"),
 }
 
 
@@ -145,6 +152,30 @@ def py_pins_pass(mod):
     for k, (s, b) in enumerate([(2.0, 0.25), (-1.0, 1.0)]):
         z = conv[0, k] * s + b
         if abs(got[0, k] - float(mpmath.mpf(z) / (1 + mpmath.exp(-mpmath.mpf(z))))) > 1e-14:
+            return False
+    return epilogue_pins_pass(mod)
+
+
+def epilogue_pins_pass(mod):
+    """The hand-derived epilogue fixture (tests/golden/epilogue_hand_cases.json)."""
+    with open(os.path.join(HERE, "golden", "epilogue_hand_cases.json")) as f:
+        ep = json.load(f)
+    with open(os.path.join(HERE, "golden", "conv_hand_cases.json")) as f:
+        conv = json.load(f)
+    case = next(c for c in conv["cases"] if c["name"] == ep["conv_case"])
+    x = conv[case["x"]] if isinstance(case["x"], str) else case["x"]
+    xb = f32_to_bf16_bits(np.asarray(x, np.float32))
+    wb = f32_to_bf16_bits(np.asarray(case["w"], np.float32))
+    for cs in ep["cases"]:
+        expected = np.asarray(cs["expected"], np.float64)
+        res = None
+        if cs["residual"]:
+            res = f32_to_bf16_bits(np.broadcast_to(np.asarray(ep["residual_per_channel"], np.float32),
+                                                   expected.shape).copy())
+        got = mod.conv_bn_act(xb, wb, np.float32(ep["gamma"]), np.float32(ep["beta"]), np.float32(ep["mean"]),
+                              np.float32(ep["var"]), ep["eps"], case["stride"], case["pad"], cs["activation"], res,
+                              threads=1)
+        if got.shape != expected.shape or not np.array_equal(got, expected):
             return False
     return True
 
