@@ -56,6 +56,15 @@ class FoldLayer(ctypes.Structure):
                 ("scale", _p), ("bias", _p)]
 
 
+class PlanRequest(ctypes.Structure):
+    """cbs_plan_request: overrides of the planner's choices (-1 / 0: planner's choice)."""
+    _fields_ = [(name, ctypes.c_int) for name in ("algo", "swap_ab", "stream_k", "pair", "block_n")]
+
+
+def _request(algo="auto", swap_ab=-1, stream_k=-1, pair=-1, block_n=0) -> PlanRequest:
+    return PlanRequest(ALGOS[algo], int(swap_ab), int(stream_k), int(pair), int(block_n))
+
+
 def _declare(name, argtypes, restype=ctypes.c_int):
     fn = getattr(_lib, name)
     fn.argtypes = argtypes
@@ -74,6 +83,9 @@ _bn_apply = _declare("conv_bn_silu_bn_apply", [_p] * 4 + [ctypes.c_longlong, _i,
 _silu_apply = _declare("conv_bn_silu_silu_apply", [_p, _p, ctypes.c_longlong, _p])
 _output_dims = _declare("conv_bn_silu_output_dims", [_i] * 8 + [ctypes.POINTER(_i)] * 2)
 _plan = _declare("conv_bn_silu_plan", [_i] * 13 + [ctypes.POINTER(PlanInfo)])
+_plan_request = _declare("conv_bn_silu_plan_request", [_i] * 11 + [ctypes.POINTER(PlanRequest), _i,
+                                                                     ctypes.POINTER(PlanInfo)])
+_forward_request = _declare("conv_bn_silu_forward_request", [_p] * 5 + [_i] * 11 + [ctypes.POINTER(PlanRequest), _p])
 _check = _declare("conv_bn_silu_check", [_p])
 _status_string = _declare("conv_bn_silu_status_string", [_i], ctypes.c_char_p)
 _last_cuda_error = _declare("conv_bn_silu_last_cuda_error", [])
@@ -137,6 +149,36 @@ def plan(n, h, w, c, c_out, r, s, stride=1, pad=0, algo="auto", sm_count: int = 
     _raise_if(_plan(n, h, w, c, c_out, r, s, sh, sw, ph, pw, ALGOS[algo], sm_count,
                     ctypes.byref(info)), "conv_bn_silu_plan")
     return info.as_dict()
+
+
+def plan_request(n, h, w, c, c_out, r, s, stride=1, pad=0, sm_count: int = 152, **overrides) -> dict:
+    """conv_bn_silu_plan_request: the plan with overrides (algo, swap_ab, stream_k, pair, block_n)."""
+    sh, sw = _pair(stride)
+    ph, pw = _pair(pad)
+    req = _request(**overrides)
+    info = PlanInfo()
+    _raise_if(_plan_request(n, h, w, c, c_out, r, s, sh, sw, ph, pw, ctypes.byref(req), sm_count,
+                            ctypes.byref(info)), "conv_bn_silu_plan_request")
+    return info.as_dict()
+
+
+def forward_request(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor, bias: torch.Tensor,
+                    stride=1, pad=0, y: torch.Tensor | None = None, stream=None, **overrides) -> torch.Tensor:
+    """conv_bn_silu_forward_request: the fused forward with the planner's choices overridden."""
+    n, h, wi, c = x.shape
+    c_out, r, s, _ = w.shape
+    sh, sw = _pair(stride)
+    ph, pw = _pair(pad)
+    ho, wo = output_dims(h, wi, r, s, (sh, sw), (ph, pw))
+    if y is None:
+        y = torch.empty((n, ho, wo, c_out), dtype=torch.bfloat16, device=x.device)
+    req = _request(**overrides)
+    st = _forward_request(_dev_tensor(x, torch.bfloat16, "x"), _dev_tensor(w, torch.bfloat16, "w"),
+                          _dev_tensor(scale, torch.float32, "scale"), _dev_tensor(bias, torch.float32, "bias"),
+                          _dev_tensor(y, torch.bfloat16, "y"), n, h, wi, c, c_out, r, s, sh, sw, ph, pw,
+                          ctypes.byref(req), _stream_handle(stream))
+    _raise_if(st, "conv_bn_silu_forward_request")
+    return y
 
 
 def fold(gamma: torch.Tensor, beta: torch.Tensor, mean: torch.Tensor, var: torch.Tensor,

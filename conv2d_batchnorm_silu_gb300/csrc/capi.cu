@@ -94,8 +94,14 @@ int sm_count_current_device(int *count)
     return CBS_OK;
 }
 
+// A request's tcgen05 overrides, or nullptr when it leaves every choice to the planner.
+bool has_overrides(const cbs::PlanRequest *rq)
+{
+    return rq && (rq->swap_ab >= 0 || rq->stream_k >= 0 || rq->pair >= 0 || rq->block_n != 0);
+}
+
 // Validated problem (pointers set) -> the chosen kernel's launch on `strm`.
-int launch_forward(const cbs::ConvProblem &p, int algo, cudaStream_t strm)
+int launch_forward(const cbs::ConvProblem &p, int algo, cudaStream_t strm, const cbs::PlanRequest *rq = nullptr)
 {
     const int chosen = select_algo(p, algo);
     if (chosen == CBS_ALGO_TCGEN05) {
@@ -104,15 +110,33 @@ int launch_forward(const cbs::ConvProblem &p, int algo, cudaStream_t strm)
         const int st = sm_count_current_device(&sms);
         if (st != CBS_OK) return st;
         if (!cbs::tc_supported(p)) {
+            if (has_overrides(rq)) return CBS_ERR_UNSUPPORTED;  // the thin-input kernel has no such choices
             cudaError_t e = cbs::gather_launch(p, sms, strm);
             return e == cudaSuccess ? CBS_OK : cuda_fail(e);
         }
-        const cbs::TcPlan plan = cbs::tc_make_plan(p, sms);
+        cbs::TcPlan plan{};
+        if (cbs::tc_make_plan_request(p, sms, rq, &plan) != 0) return CBS_ERR_UNSUPPORTED;
         cudaError_t e = cbs::tc_launch(p, plan, strm);
         return e == cudaSuccess ? CBS_OK : cuda_fail(e);
     }
+    if (has_overrides(rq)) return CBS_ERR_UNSUPPORTED;
     cudaError_t e = cbs::direct_launch(p, strm);
     return e == cudaSuccess ? CBS_OK : cuda_fail(e);
+}
+
+// cbs_plan_request -> checked algorithm and planner overrides.
+int read_request(const cbs_plan_request *req, int *algo, cbs::PlanRequest *rq)
+{
+    if (!req) return CBS_ERR_INVALID_ARG;
+    if (req->algo < CBS_ALGO_AUTO || req->algo > CBS_ALGO_DIRECT) return CBS_ERR_INVALID_ARG;
+    for (int v : {req->swap_ab, req->stream_k, req->pair})
+        if (v < -1 || v > 1) return CBS_ERR_INVALID_ARG;
+    if (req->block_n != 0 && req->block_n != 16 && req->block_n != 32 && req->block_n != 64 &&
+        req->block_n != 128 && req->block_n != 256)
+        return CBS_ERR_INVALID_ARG;
+    *algo = req->algo;
+    *rq = cbs::PlanRequest{req->swap_ab, req->stream_k, req->pair, req->block_n};
+    return CBS_OK;
 }
 
 // ------------------------------------------------------------------ allocation-free forward
@@ -344,19 +368,16 @@ int conv_bn_silu_output_dims(int h, int w_in, int r, int s, int stride_h, int st
     return dims_from(h, w_in, r, s, stride_h, stride_w, pad_h, pad_w, ho, wo);
 }
 
-int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, int stride_h, int stride_w,
-                      int pad_h, int pad_w, int algo, int sm_count, cbs_plan_info *info)
+static int fill_plan(const cbs::ConvProblem &p, int algo, int sm_count, const cbs::PlanRequest *rq,
+                     cbs_plan_info *info)
 {
-    if (!info || sm_count < 1 || algo < CBS_ALGO_AUTO || algo > CBS_ALGO_DIRECT)
-        return CBS_ERR_INVALID_ARG;
-    cbs::ConvProblem p{};
-    const int st = make_problem(n, h, w_in, c, c_out, r, s, stride_h, stride_w, pad_h, pad_w, &p);
-    if (st != CBS_OK) return st;
+    const int n = p.n, c = p.c, c_out = p.c_out, r = p.r, s = p.s;
+    (void)n;
     const int chosen = select_algo(p, algo);
     cbs_plan_info out{};
     out.algo = chosen;
     if (chosen == CBS_ALGO_TCGEN05 && !cbs::tc_supported(p)) {
-        if (!cbs::gather_supported(p)) return CBS_ERR_UNSUPPORTED;
+        if (!cbs::gather_supported(p) || has_overrides(rq)) return CBS_ERR_UNSUPPORTED;
         // Thin-input kernel: one 128-pixel tile per MMA step, K zero-padded to 32 or 64.
         const int taps = r * s * c;
         const int n16 = (c_out + 15) / 16 * 16;
@@ -372,7 +393,8 @@ int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, in
         out.k_iters = 1;
         out.cluster = 1;
     } else if (chosen == CBS_ALGO_TCGEN05) {
-        const cbs::TcPlan t = cbs::tc_make_plan(p, sm_count);
+        cbs::TcPlan t{};
+        if (cbs::tc_make_plan_request(p, sm_count, rq, &t) != 0) return CBS_ERR_UNSUPPORTED;
         out.block_m = t.swap_ab ? t.block_n : cbs::kTcBlockM;  // output pixels per tile
         out.block_n = t.swap_ab ? cbs::kTcBlockM : t.block_n;  // output channels per tile
         out.block_k = t.block_k;
@@ -387,6 +409,7 @@ int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, in
         out.cluster = t.pair ? 2 : 1;
         out.workspace_bytes = t.workspace_bytes;
     } else {
+        if (has_overrides(rq)) return CBS_ERR_UNSUPPORTED;  // the direct kernel has no tilings to choose
         const long long bx = (p.m + cbs::kDirectThreads - 1) / cbs::kDirectThreads;
         const int by = (c_out + cbs::kDirectBlockN - 1) / cbs::kDirectBlockN;
         out.block_m = cbs::kDirectThreads;
@@ -401,6 +424,56 @@ int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, in
     }
     *info = out;
     return CBS_OK;
+}
+
+int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, int stride_h, int stride_w,
+                      int pad_h, int pad_w, int algo, int sm_count, cbs_plan_info *info)
+{
+    if (!info || sm_count < 1 || algo < CBS_ALGO_AUTO || algo > CBS_ALGO_DIRECT)
+        return CBS_ERR_INVALID_ARG;
+    cbs::ConvProblem p{};
+    const int st = make_problem(n, h, w_in, c, c_out, r, s, stride_h, stride_w, pad_h, pad_w, &p);
+    if (st != CBS_OK) return st;
+    return fill_plan(p, algo, sm_count, nullptr, info);
+}
+
+int conv_bn_silu_plan_request(int n, int h, int w_in, int c, int c_out, int r, int s, int stride_h,
+                              int stride_w, int pad_h, int pad_w, const cbs_plan_request *req, int sm_count,
+                              cbs_plan_info *info)
+{
+    if (!info || sm_count < 1) return CBS_ERR_INVALID_ARG;
+    int algo = 0;
+    cbs::PlanRequest rq{};
+    int st = read_request(req, &algo, &rq);
+    if (st != CBS_OK) return st;
+    cbs::ConvProblem p{};
+    st = make_problem(n, h, w_in, c, c_out, r, s, stride_h, stride_w, pad_h, pad_w, &p);
+    if (st != CBS_OK) return st;
+    return fill_plan(p, algo, sm_count, &rq, info);
+}
+
+int conv_bn_silu_forward_request(const void *x, const void *w, const float *scale, const float *bias,
+                                 void *y, int n, int h, int w_in, int c, int c_out, int r, int s,
+                                 int stride_h, int stride_w, int pad_h, int pad_w, const cbs_plan_request *req,
+                                 void *stream)
+{
+    int algo = 0;
+    cbs::PlanRequest rq{};
+    int st = read_request(req, &algo, &rq);
+    if (st != CBS_OK) return st;
+    cbs::ConvProblem p{};
+    st = make_problem(n, h, w_in, c, c_out, r, s, stride_h, stride_w, pad_h, pad_w, &p);
+    if (st != CBS_OK) return st;
+    if (p.m == 0 || c_out == 0) return CBS_OK;
+    if (!x || !w || !scale || !bias || !y) return CBS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(scale) || !aligned16(bias) || !aligned16(y))
+        return CBS_ERR_MISALIGNED;
+    p.x = x;
+    p.w = w;
+    p.scale = scale;
+    p.bias = bias;
+    p.y = y;
+    return launch_forward(p, algo, static_cast<cudaStream_t>(stream), &rq);
 }
 
 int conv_bn_silu_check(void *stream)

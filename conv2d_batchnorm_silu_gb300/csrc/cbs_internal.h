@@ -100,6 +100,13 @@ cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // Planning (host only, no GPU needed).
 bool tc_supported(const ConvProblem &p);
 TcPlan tc_make_plan(const ConvProblem &p, int sm_count);
+// Overrides of the planner's tcgen05 choices: -1 (block_n: 0) leaves a choice to the planner.
+struct PlanRequest {
+    int swap_ab, stream_k, pair, block_n;
+};
+// As tc_make_plan with the overrides in `rq` (nullable); -1 when the kernel cannot run
+// them on this shape (e.g. stream-K shares shorter than one tile).
+int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *rq, TcPlan *out);
 // Dynamic shared memory of the tcgen05 kernel; `pair`: a 2-CTA pair holds half of each weight tile per CTA.
 int tc_smem_bytes(int block_n, int block_k, int stages, int pair);
 

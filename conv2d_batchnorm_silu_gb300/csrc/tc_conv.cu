@@ -1066,8 +1066,13 @@ bool tc_supported(const ConvProblem &p)
     return true;
 }
 
-TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
+static bool valid_block_n(int bn) { return bn == 16 || bn == 32 || bn == 64 || bn == 128 || bn == 256; }
+
+int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *rq, TcPlan *out)
 {
+    const PlanRequest dflt{-1, -1, -1, 0};
+    const PlanRequest &q = rq ? *rq : dflt;
+    if (q.block_n != 0 && !valid_block_n(q.block_n)) return -1;
     TcPlan t{};
     t.block_k = p.c % 64 == 0 ? 64 : (p.c % 32 == 0 ? 32 : 16);
     t.c_chunks = (p.c + t.block_k - 1) / t.block_k;
@@ -1100,7 +1105,10 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
     const long long ptiles256 = (p.m + 255) / 256;
     const bool long_k_wide = p.c_out > 128 && t.block_n == 256 && t.k_iters >= 16;
     t.swap_ab = (p.c_out > 64 && p.c_out <= 256 && !long_k_wide && ptiles256 >= sm_count / 2) ? 1 : 0;
+    if (q.swap_ab >= 0) t.swap_ab = q.swap_ab ? 1 : 0;
     if (t.swap_ab) {
+        // The channel-major tile is 128 channels x 256 pixels, whole tiles only.
+        if ((q.block_n != 0 && q.block_n != 256) || q.stream_k == 1 || q.pair == 1) return -1;
         t.block_n = 256;
         t.stages = stages_for(256, t.block_k);
         t.m_tiles = (int)ptiles256;
@@ -1112,8 +1120,10 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
         t.pair = 0;
         t.workspace_bytes = 0;
         t.flag_bytes = 0;
-        return t;
+        *out = t;
+        return 0;
     }
+    if (q.block_n != 0) t.block_n = q.block_n;
     t.stages = stages_for(t.block_n, t.block_k);
     t.m_tiles = m_tiles;
     t.n_tiles = (p.c_out + t.block_n - 1) / t.block_n;
@@ -1124,10 +1134,16 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
     // takes total/grid consecutive K steps.  Each share must cover at least one
     // tile so that a tile is split between two CTAs at most.
     const long long total = (long long)t.tiles * t.k_iters;
+    const bool sk_possible = total / sm_count >= t.k_iters;
     t.stream_k = (t.tiles > sm_count && t.tiles % sm_count != 0 && t.tiles < 4LL * sm_count &&
-                  t.k_iters >= 16 && total / sm_count >= t.k_iters)
+                  t.k_iters >= 16 && sk_possible)
                      ? 1
                      : 0;
+    if (q.stream_k >= 0) {
+        if (q.stream_k == 1 && !sk_possible) return -1;
+        t.stream_k = q.stream_k ? 1 : 0;
+    }
+    if (q.pair == 1 && !t.stream_k) return -1;  // pairs are stream-K workers
     t.workspace_bytes = 0;
     t.flag_bytes = 0;
     t.pair = 0;
@@ -1135,9 +1151,14 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
         t.grid = sm_count;
         // Pairs of CTAs (clusters of two) run the 2-CTA MMA on pair tiles of
         // 256 x 256, each CTA holding half of the weight tile: the stream-K worker
-        // is then the pair.
+        // is then the pair.  Each pair's share must cover at least one pair tile.
         const int pair_tiles = (t.m_tiles + 1) / 2 * t.n_tiles;
-        t.pair = (t.block_n == 256 && sm_count % 2 == 0 && pair_tiles >= sm_count / 2) ? 1 : 0;
+        const bool pair_possible = t.block_n == 256 && sm_count % 2 == 0 && pair_tiles >= sm_count / 2;
+        t.pair = pair_possible ? 1 : 0;
+        if (q.pair >= 0) {
+            if (q.pair == 1 && !pair_possible) return -1;
+            t.pair = q.pair ? 1 : 0;
+        }
         if (t.pair) {
             t.tiles = pair_tiles;  // the kernel's work units
             t.stages = stages_for(t.block_n, t.block_k, 1);
@@ -1147,6 +1168,14 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
         t.flag_bytes = (slots * kTcFlagsPerSlot * (long long)sizeof(int) + 255) / 256 * 256;
         t.workspace_bytes = t.flag_bytes + slots * kTcBlockM * t.block_n * 4;
     }
+    *out = t;
+    return 0;
+}
+
+TcPlan tc_make_plan(const ConvProblem &p, int sm_count)
+{
+    TcPlan t{};
+    tc_make_plan_request(p, sm_count, nullptr, &t);  // the planner's own choices always succeed
     return t;
 }
 

@@ -232,6 +232,35 @@ int conv_bn_silu_plan(int n, int h, int w_in, int c, int c_out, int r, int s, in
                       int stride_w, int pad_h, int pad_w, int algo, int sm_count,
                       cbs_plan_info *info);
 
+/*
+ * Overrides of the planner's choices, for measuring the alternatives on a
+ * given shape ("Fusing an Epilogue", section "Three kernels for one
+ * operation": which kernel and tile run is a threshold somebody measures and
+ * writes down).  -1 (block_n: 0) leaves that choice to the planner.
+ */
+typedef struct cbs_plan_request {
+    int algo;     /* cbs_algo */
+    int swap_ab;  /* -1, or 0: pixel-major tiles, 1: channel-major tiles (swap AB: 128 channels x 256 pixels) */
+    int stream_k; /* -1, or 0: whole tiles per CTA, 1: K steps split evenly over the grid */
+    int pair;     /* -1, or 0: single CTAs, 1: 2-CTA pairs (256-wide pixel-major tiles with stream-K only) */
+    int block_n;  /* 0, or 16/32/64/128/256 output channels per pixel-major tile */
+} cbs_plan_request;
+
+/* conv_bn_silu_plan with overrides.  CBS_ERR_INVALID_ARG for an out-of-range
+ * field; CBS_ERR_UNSUPPORTED when the kernel cannot run the combination on
+ * this shape (e.g. stream-K with shares shorter than one tile, pairs without
+ * stream-K, any tcgen05 override on the thin-input or direct kernels). */
+int conv_bn_silu_plan_request(int n, int h, int w_in, int c, int c_out, int r, int s, int stride_h,
+                              int stride_w, int pad_h, int pad_w, const cbs_plan_request *req, int sm_count,
+                              cbs_plan_info *info);
+
+/* conv_bn_silu_forward_algo with overrides (req->algo replaces `algo`); the
+ * same result within the layer's tolerance, whatever the tiling. */
+int conv_bn_silu_forward_request(const void *x, const void *w, const float *scale, const float *bias,
+                                 void *y, int n, int h, int w_in, int c, int c_out, int r, int s,
+                                 int stride_h, int stride_w, int pad_h, int pad_w, const cbs_plan_request *req,
+                                 void *stream);
+
 /* Synchronises `stream`, then reads and clears the library's device error word.
  * Returns CBS_ERR_TIMEOUT if any kernel since the last check gave up on a
  * pipeline wait, CBS_ERR_CUDA if the synchronisation failed, else CBS_OK. */

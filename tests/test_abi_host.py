@@ -181,3 +181,45 @@ def test_status_strings(lib):
     for st in range(6):
         assert isinstance(lib._status_string(st), bytes) and lib._status_string(st)
     assert lib._status_string(99) == b"unknown status"
+
+
+def test_plan_request_overrides(lib):
+    """Planner overrides: each forced choice shows in the plan, and combinations the
+    kernels cannot run are refused before anything launches."""
+    deep = (32, 20, 20, 512, 512, 3, 3, 1, 1)
+    assert lib.plan_request(*deep)["cluster"] == 2                       # the planner's own choice
+    p = lib.plan_request(*deep, pair=0)
+    assert p["cluster"] == 1 and p["stream_k"] == 1
+    p = lib.plan_request(*deep, stream_k=0)
+    assert p["stream_k"] == 0 and p["cluster"] == 1 and p["workspace_bytes"] == 0
+    p = lib.plan_request(*deep, block_n=128, stream_k=0)
+    assert p["block_n"] == 128 and p["tiles"] == 400
+    down = (16, 160, 160, 64, 128, 3, 3, 2, 1)
+    assert lib.plan_request(*down)["swap_ab"] == 1
+    p = lib.plan_request(*down, swap_ab=0)
+    assert p["swap_ab"] == 0 and p["block_n"] == 128
+    assert lib.plan_request(*down, algo="direct")["algo"] == "direct"
+    for bad in ({"swap_ab": 1, "stream_k": 1}, {"swap_ab": 1, "block_n": 128}, {"pair": 1, "stream_k": 0},
+                {"algo": "direct", "swap_ab": 0}):
+        with pytest.raises(lib.CbsError):
+            lib.plan_request(*down, **bad)
+    with pytest.raises(lib.CbsError):                                     # stream-K shares < one tile
+        lib.plan_request(1, 32, 32, 16, 32, 3, 3, 1, 1, stream_k=1)
+    with pytest.raises(lib.CbsError):                                     # thin-input kernel: no tilings
+        lib.plan_request(1, 640, 640, 3, 16, 3, 3, 2, 1, swap_ab=0)
+    for bad in ({"swap_ab": 2}, {"pair": -2}, {"block_n": 48}):
+        with pytest.raises(lib.CbsError) as e:
+            lib.plan_request(*down, **bad)
+        assert e.value.status == lib.CBS_ERR_INVALID_ARG
+
+
+def test_tuning_sweep_variants_are_consistent():
+    from conv2d_batchnorm_silu_gb300 import tune
+    vs = list(tune.variants())
+    labels = [v[0] for v in vs]
+    assert len(labels) == len(set(labels)) and labels[:2] == ["auto", "direct"]
+    for label, ov in vs[2:]:
+        assert not (ov["pair"] and not ov["stream_k"])
+        assert not (ov["swap_ab"] and (ov["stream_k"] or ov["pair"]))
+    assert len(tune.SWEEP) >= 15 and len({s.name for s in tune.SWEEP}) == len(tune.SWEEP)
+

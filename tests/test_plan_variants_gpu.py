@@ -1,0 +1,62 @@
+"""Tilings forced through conv_bn_silu_forward_request (GPU only): every
+alternative the planner can be overridden into must compute the same layer.
+Each case runs a tcgen05 tiling the planner would not pick for that shape and
+compares every output element with the fp64 oracle at the layer's tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conv2d_batchnorm_silu_gb300.synthetic import (LayerShape, bf16_bits_to_f32, bits_to_torch_bf16,
+                                                   make_layer_inputs, torch_bf16_to_bits)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def capi():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from conv2d_batchnorm_silu_gb300 import _build
+    _build.build()
+    from conv2d_batchnorm_silu_gb300 import capi as c
+    return c
+
+
+CASES = [
+    ("pairs_off", LayerShape("sk", 31, 20, 20, 128, 512, 3, 3, 1, 1), {"pair": 0}),
+    ("streamk_off", LayerShape("sk", 31, 20, 20, 128, 512, 3, 3, 1, 1), {"stream_k": 0}),
+    ("n128_whole", LayerShape("sk", 31, 20, 20, 128, 512, 3, 3, 1, 1), {"stream_k": 0, "block_n": 128}),
+    ("n128_streamk", LayerShape("sk", 31, 20, 20, 128, 512, 3, 3, 1, 1), {"stream_k": 1, "block_n": 128}),
+    ("swap_off_tail", LayerShape("sw", 2, 100, 100, 16, 80, 3, 3, 1, 1), {"swap_ab": 0}),
+    ("pw_n256", LayerShape("pw", 16, 40, 40, 256, 256, 1, 1, 1, 0), {"swap_ab": 0, "block_n": 256}),
+    ("pw_n64", LayerShape("pw", 4, 40, 40, 256, 256, 1, 1, 1, 0), {"swap_ab": 0, "block_n": 64}),
+    ("swap_small", LayerShape("ss", 2, 13, 11, 16, 24, 3, 3, 1, 1), {"swap_ab": 1}),
+    ("direct", LayerShape("dd", 2, 13, 11, 16, 24, 3, 3, 1, 1), {"algo": "direct"}),
+]
+
+
+@pytest.mark.parametrize("name,shape,overrides", CASES, ids=[c[0] for c in CASES])
+def test_forced_tiling_matches_oracle(capi, name, shape, overrides):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    forced = capi.plan_request(shape.n, shape.h, shape.w, shape.c, shape.k, shape.r, shape.s, shape.stride,
+                               shape.pad, sms, **overrides)
+    auto = capi.plan(shape.n, shape.h, shape.w, shape.c, shape.k, shape.r, shape.s, shape.stride, shape.pad,
+                     "auto", sms)
+    assert forced != auto, "the override must change the plan"
+    dev = torch.device("cuda:0")
+    inp = make_layer_inputs(shape, seed=61)
+    x = bits_to_torch_bf16(inp.x_bits).to(dev)
+    w = bits_to_torch_bf16(inp.w_bits).to(dev)
+    g, b, m, v = (torch.from_numpy(a).to(dev) for a in (inp.gamma, inp.beta, inp.mean, inp.var))
+    scale, bias = capi.fold(g, b, m, v, inp.eps)
+    y = capi.forward_request(x, w, scale, bias, shape.stride, shape.pad, **overrides)
+    torch.cuda.synchronize()
+    capi.check()
+    got = bf16_bits_to_f32(torch_bf16_to_bits(y)).astype(np.float64)
+    ref = oracle.conv_bn_silu(inp.x_bits, inp.w_bits, inp.gamma, inp.beta, inp.mean, inp.var, inp.eps,
+                              shape.stride, shape.pad)
+    err = np.abs(got - ref)
+    bound = 1e-2 + 1e-2 * np.abs(ref)
+    assert np.all(np.isfinite(got))
+    assert np.all(err <= bound), (name, float((err - bound).max()))
