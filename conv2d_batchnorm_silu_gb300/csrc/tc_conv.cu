@@ -1099,12 +1099,21 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
             }
         }
     }
-    // Swap AB for 65..256 output channels (unless the long-K path above took the
-    // 256-wide pixel-major tile): the tile becomes 128 channels x 256 pixels so
-    // that every MMA runs at N = 256.
+    // Swap AB for 32..256 output channels: the tile becomes 128 channels x 256
+    // pixels so that every MMA runs at N = 256.  Thresholds from a measured sweep
+    // of YOLO-shaped layers (the package's tune module): swapped tiles win on
+    // 3x3 layers from 32 output channels up and on 1x1 layers from 128, as long
+    // as there are tiles for at least half the SMs; they lose where the long-K
+    // path above runs 256-wide pair tiles with stream-K, and on 1x1 layers with
+    // at most 64 output channels (one or two K steps: the transposing epilogue
+    // costs more than the wider MMA saves).
     const long long ptiles256 = (p.m + 255) / 256;
-    const bool long_k_wide = p.c_out > 128 && t.block_n == 256 && t.k_iters >= 16;
-    t.swap_ab = (p.c_out > 64 && p.c_out <= 256 && !long_k_wide && ptiles256 >= sm_count / 2) ? 1 : 0;
+    const long long swap_tiles = ptiles256 * ((p.c_out + kTcBlockM - 1) / kTcBlockM);
+    const bool pair_path = p.c_out > 128 && t.k_iters >= 16 && tiles256 >= sm_count;
+    const bool short_narrow = p.c_out <= 64 && t.k_iters <= 2;
+    t.swap_ab = (p.c_out >= 32 && p.c_out <= 256 && !pair_path && !short_narrow && swap_tiles >= sm_count / 2)
+                    ? 1
+                    : 0;
     if (q.swap_ab >= 0) t.swap_ab = q.swap_ab ? 1 : 0;
     if (t.swap_ab) {
         // The channel-major tile is 128 channels x 256 pixels, whole tiles only.
