@@ -532,8 +532,14 @@ def epilogue_variants(capi, sets, layers, stream, dev, iters, silu_us) -> dict:
 
 def run_e2e(args, capi, inputs, dev, stream, world):
     """Same metric through the public API with host buffers: per step, every layer's x goes
-    host->device from pinned memory, the batched fold and the fused forwards run, and y comes back
-    device->host into pinned memory.  Weights and BN statistics stay resident on the device."""
+    host->device from pinned memory, the batched fold and the fused forwards run, and y comes
+    back device->host into pinned memory.  Weights and BN statistics stay resident on the device.
+
+    The copies run on their own streams (one per direction) so that layer i+1's upload and
+    layer i-1's download overlap layer i's forward; events order each buffer's upload, forward
+    and download, across steps too (a step's upload of x waits for the previous step's forward
+    on that buffer, a forward waits for the previous download of its y).  The serial form (all
+    on one stream) is reported beside it."""
     layers = args.layers
     host_x = {n: bits_to_torch_bf16(inputs[n].x_bits).pin_memory() for n in layers}
     bufs = {n: LayerBuffers(inputs[n], dev) for n in layers}
@@ -541,37 +547,78 @@ def run_e2e(args, capi, inputs, dev, stream, world):
     h2d = sum(t.numel() * 2 for t in host_x.values())
     d2h = sum(t.numel() * 2 for t in host_y.values())
     flops_step = sum(LAYERS[n].flops for n in layers)
-
     fold = capi.FoldBatch([(b.g, b.b, b.m, b.v, b.eps, b.scale, b.bias) for b in (bufs[n] for n in layers)])
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    uploaded = {n: torch.cuda.Event() for n in layers}
+    computed = {n: torch.cuda.Event() for n in layers}
+    downloaded = {n: torch.cuda.Event() for n in layers}
 
-    def step():
+    def forward(n):
+        b = bufs[n]
+        sh = b.shape
+        capi.forward(b.x, b.w, b.scale, b.bias, sh.stride, sh.pad, y=b.y, stream=stream)
+
+    def step_serial():
         with torch.cuda.stream(stream):
             fold(stream)
             for n in layers:
-                b = bufs[n]
-                sh = b.shape
-                b.x.copy_(host_x[n], non_blocking=True)
-                capi.forward(b.x, b.w, b.scale, b.bias, sh.stride, sh.pad, y=b.y, stream=stream)
-                host_y[n].copy_(b.y, non_blocking=True)
+                bufs[n].x.copy_(host_x[n], non_blocking=True)
+                forward(n)
+                host_y[n].copy_(bufs[n].y, non_blocking=True)
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    s.record(stream)
-    for _ in range(args.e2e_steps):
-        step()
-    e.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    t = max_over_ranks(s.elapsed_time(e) / 1e3, world, dev)
+    def step_pipelined():
+        for n in layers:
+            s_in.wait_event(computed[n])          # the previous step's forward has read x
+            with torch.cuda.stream(s_in):
+                bufs[n].x.copy_(host_x[n], non_blocking=True)
+            uploaded[n].record(s_in)
+        with torch.cuda.stream(stream):
+            fold(stream)
+            for n in layers:
+                stream.wait_event(uploaded[n])
+                stream.wait_event(downloaded[n])  # the previous step's download of y is done
+                forward(n)
+                computed[n].record(stream)
+        for n in layers:
+            s_out.wait_event(computed[n])
+            with torch.cuda.stream(s_out):
+                host_y[n].copy_(bufs[n].y, non_blocking=True)
+            downloaded[n].record(s_out)
+
+    def timed(step):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        s.record(stream)
+        s_in.wait_event(s)
+        for _ in range(args.e2e_steps):
+            step()
+        for st in (s_in, s_out):                   # join every stream before the end event
+            ev = torch.cuda.Event()
+            ev.record(st)
+            stream.wait_event(ev)
+        e.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(s.elapsed_time(e) / 1e3, world, dev)
+
+    t_serial = timed(step_serial)
+    t = timed(step_pipelined)
+    # The last step's results are in host memory: check one layer against the device copy.
+    last = layers[-1]
+    assert torch.equal(host_y[last], bufs[last].y.cpu()), "e2e: downloaded y differs from the device's"
     return {"value": round(aggregate_throughput(flops_step * args.e2e_steps, world, t) / 1e12, 3),
             "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(t / args.e2e_steps * 1e3, 4), "steps": args.e2e_steps,
-            "api": "conv2d_batchnorm_silu_gb300.capi.FoldBatch/forward on the C ABI, pinned host buffers"}
+            "serial_value": round(aggregate_throughput(flops_step * args.e2e_steps, world, t_serial) / 1e12, 3),
+            "serial_ms_per_step": round(t_serial / args.e2e_steps * 1e3, 4),
+            "api": "conv2d_batchnorm_silu_gb300.capi.FoldBatch/forward on the C ABI, pinned host buffers; "
+                   "uploads and downloads on their own streams, overlapping the forwards"}
 
 
 # ------------------------------------------------------------------ the oracle (CPU) legs
