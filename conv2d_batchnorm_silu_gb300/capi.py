@@ -57,12 +57,14 @@ class FoldLayer(ctypes.Structure):
 
 
 class PlanRequest(ctypes.Structure):
-    """cbs_plan_request: overrides of the planner's choices (-1 / 0: planner's choice)."""
-    _fields_ = [(name, ctypes.c_int) for name in ("algo", "swap_ab", "stream_k", "pair", "block_n")]
+    """cbs_plan_request: overrides of the planner's choices (-1 / 0: planner's choice) and the
+    bound on the tcgen05 kernel's pipeline waits (0: the 2 s default)."""
+    _fields_ = [(name, ctypes.c_int) for name in ("algo", "swap_ab", "stream_k", "pair", "block_n")] + \
+        [("wait_timeout_ns", ctypes.c_longlong)]
 
 
-def _request(algo="auto", swap_ab=-1, stream_k=-1, pair=-1, block_n=0) -> PlanRequest:
-    return PlanRequest(ALGOS[algo], int(swap_ab), int(stream_k), int(pair), int(block_n))
+def _request(algo="auto", swap_ab=-1, stream_k=-1, pair=-1, block_n=0, wait_timeout_ns=0) -> PlanRequest:
+    return PlanRequest(ALGOS[algo], int(swap_ab), int(stream_k), int(pair), int(block_n), int(wait_timeout_ns))
 
 
 def _declare(name, argtypes, restype=ctypes.c_int):

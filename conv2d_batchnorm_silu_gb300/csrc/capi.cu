@@ -128,6 +128,7 @@ int launch_forward(const cbs::ConvProblem &p, int algo, cudaStream_t strm, const
 int read_request(const cbs_plan_request *req, int *algo, cbs::PlanRequest *rq)
 {
     if (!req) return CBS_ERR_INVALID_ARG;
+    if (req->wait_timeout_ns < 0) return CBS_ERR_INVALID_ARG;
     if (req->algo < CBS_ALGO_AUTO || req->algo > CBS_ALGO_DIRECT) return CBS_ERR_INVALID_ARG;
     for (int v : {req->swap_ab, req->stream_k, req->pair})
         if (v < -1 || v > 1) return CBS_ERR_INVALID_ARG;
@@ -473,6 +474,7 @@ int conv_bn_silu_forward_request(const void *x, const void *w, const float *scal
     p.scale = scale;
     p.bias = bias;
     p.y = y;
+    p.wait_timeout_ns = req->wait_timeout_ns;
     return launch_forward(p, algo, static_cast<cudaStream_t>(stream), &rq);
 }
 

@@ -29,6 +29,7 @@ struct ConvProblem {
     long long m;    // output pixels
     int epi_mode;          // EpiMode: SiLU (the layer), conv only, BN only, BN + ReLU
     const void *residual;  // nullable bf16 NHWC [m][c_out], added after the activation
+    long long wait_timeout_ns;  // > 0: bound on the tcgen05 kernel's pipeline waits (0: the 2 s default)
 };
 
 // Tile configuration of the tcgen05 implicit GEMM.

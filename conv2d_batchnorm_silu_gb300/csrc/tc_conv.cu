@@ -55,6 +55,7 @@ struct TcArgs {
     int epi_mode;    // EpiMode applied to the accumulator
     const __nv_bfloat16 *residual;  // nullable: bf16 [m][c_out] added after the activation
     int stream_k;    // 1: each CTA takes an equal share of all K steps (see WorkIter)
+    unsigned long long wait_ns;  // bound on every pipeline wait (draining copies in flight keeps 2 s)
     float *partial;  // stream-K: [grid-1][128*BN] fp32 partial tiles (slot c: boundary of CTAs c, c+1)
     int *flags;      // stream-K: per slot, a ready flag and an arrival ticket per epilogue warp; 0 between launches
 };
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 bool ok = true;
                 for (int it = u.kb; it < u.ke; ++it) {
                     const uint32_t e_bar = dev::smem_u32(&empty[stage]);
-                    if (!dev::mbar_wait_bounded(e_bar, phase ^ 1u, abort_flag, kWaitTimeoutNs)) {
+                    if (!dev::mbar_wait_bounded(e_bar, phase ^ 1u, abort_flag, a.wait_ns)) {
                         if (!*abort_flag) record_error(kErrTimeoutProducer, abort_flag);
                         ok = false;
                         break;
@@ -397,11 +398,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // Every load issued must land before the CTA may exit.  The odd CTA of a
             // pair cannot see the full barrier its loads complete on; its loads have
             // landed once the MMAs that read them released the stage.
-            for (int i = 0; i < STAGES; ++i) {
+            // After one drain wait has run out (2 s), the copies issued before it have long
+            // landed: the remaining stages are not waited for again.
+            bool drain_ok = true;
+            for (int i = 0; i < STAGES && drain_ok; ++i) {
                 if ((issued >> i) & 1u) {
                     const uint32_t bar = (PAIR && rank != 0) ? dev::smem_u32(&empty[i]) : dev::smem_u32(&full[i]);
-                    if (!dev::mbar_wait_bounded(bar, (issued_parity >> i) & 1u, nullptr, kWaitTimeoutNs))
+                    if (!dev::mbar_wait_bounded(bar, (issued_parity >> i) & 1u, nullptr, kWaitTimeoutNs)) {
                         record_error(kErrTimeoutDrain, abort_flag);
+                        drain_ok = false;
+                    }
                 }
             }
         }
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int buf = lt & 1;
                 const uint32_t tparity = (uint32_t)(lt >> 1) & 1u;
                 if (!dev::mbar_wait_bounded(dev::smem_u32(&tempty[buf]), tparity ^ 1u, abort_flag,
-                                            kWaitTimeoutNs)) {
+                                            a.wait_ns)) {
                     if (!*abort_flag) record_error(kErrTimeoutMma, abort_flag);
                     break;
                 }
@@ -434,7 +440,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
                 for (int it = u.kb; it < u.ke; ++it) {
                     if (!dev::mbar_wait_bounded(dev::smem_u32(&full[stage]), phase, abort_flag,
-                                                kWaitTimeoutNs)) {
+                                                a.wait_ns)) {
                         if (!*abort_flag) record_error(kErrTimeoutMma, abort_flag);
                         ok = false;
                         break;
@@ -518,7 +524,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int ok = 1;
             if (lane == 0)
                 ok = dev::mbar_wait_bounded(dev::smem_u32(&tfull[buf]), tparity, abort_flag,
-                                            kWaitTimeoutNs)
+                                            a.wait_ns)
                          ? 1
                          : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -618,7 +624,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (combine) {
                 int got = 1;
                 if (lane == 0)
-                    got = wait_flag_bounded(a.flags + slot * kTcFlagsPerSlot + ep, abort_flag, kWaitTimeoutNs) ? 1 : 0;
+                    got = wait_flag_bounded(a.flags + slot * kTcFlagsPerSlot + ep, abort_flag, a.wait_ns) ? 1 : 0;
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!got) {
                     if (lane == 0 && !*abort_flag) record_error(kErrTimeoutEpilogue, abort_flag);
@@ -1012,6 +1018,7 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
     a.epi_mode = p.epi_mode;
     a.residual = static_cast<const __nv_bfloat16 *>(p.residual);
     a.stream_k = plan.stream_k;
+    a.wait_ns = p.wait_timeout_ns > 0 ? (unsigned long long)p.wait_timeout_ns : kWaitTimeoutNs;
     a.partial = nullptr;
     a.flags = nullptr;
     if (plan.stream_k) {

@@ -244,6 +244,13 @@ typedef struct cbs_plan_request {
     int stream_k; /* -1, or 0: whole tiles per CTA, 1: K steps split evenly over the grid */
     int pair;     /* -1, or 0: single CTAs, 1: 2-CTA pairs (256-wide pixel-major tiles with stream-K only) */
     int block_n;  /* 0, or 16/32/64/128/256 output channels per pixel-major tile */
+    long long wait_timeout_ns; /* 0: the default bound (2 s) on every pipeline wait of the tcgen05
+                                  kernel; > 0: that bound instead.  A kernel whose wait runs out
+                                  records it, stops, waits for its own copies in flight, frees its
+                                  tensor memory and returns: conv_bn_silu_check then reports
+                                  CBS_ERR_TIMEOUT, and later calls run normally.  (A bound of a
+                                  few nanoseconds makes the waits run out on purpose: the watchdog
+                                  test.)  Ignored by the other kernels. */
 } cbs_plan_request;
 
 /* conv_bn_silu_plan with overrides.  CBS_ERR_INVALID_ARG for an out-of-range

@@ -207,7 +207,7 @@ def test_plan_request_overrides(lib):
         lib.plan_request(1, 32, 32, 16, 32, 3, 3, 1, 1, stream_k=1)
     with pytest.raises(lib.CbsError):                                     # thin-input kernel: no tilings
         lib.plan_request(1, 640, 640, 3, 16, 3, 3, 2, 1, swap_ab=0)
-    for bad in ({"swap_ab": 2}, {"pair": -2}, {"block_n": 48}):
+    for bad in ({"swap_ab": 2}, {"pair": -2}, {"block_n": 48}, {"wait_timeout_ns": -1}):
         with pytest.raises(lib.CbsError) as e:
             lib.plan_request(*down, **bad)
         assert e.value.status == lib.CBS_ERR_INVALID_ARG
