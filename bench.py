@@ -498,8 +498,9 @@ def fusion_comparison(capi, sets, layers, stream, dev, iters, fused_us) -> dict:
 
 def epilogue_variants(capi, sets, layers, stream, dev, iters, silu_us) -> dict:
     """Each layer timed alone (L2 flushed before every call) with the other epilogues of
-    conv_bn_act_forward: BN only, BN + ReLU, and BN + SiLU + a residual add (which reads a
-    second output-sized tensor), next to the fused SiLU layer itself."""
+    conv_bn_act_forward: BN only, BN + ReLU, BN + SiLU + a residual add (which reads a second
+    output-sized tensor) and BN + SiLU with an fp8 e4m3 output (conv_bn_act_forward_fp8), next
+    to the fused SiLU layer itself."""
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     out = {}
     with torch.cuda.stream(stream):
@@ -507,8 +508,9 @@ def epilogue_variants(capi, sets, layers, stream, dev, iters, silu_us) -> dict:
             sh = LAYERS[n]
             res = torch.randn((sh.n, sh.ho, sh.wo, sh.k), device=dev).to(torch.bfloat16)
             row = {"silu_us": round(silu_us[n], 3)}
+            y8 = torch.empty((sh.n, sh.ho, sh.wo, sh.k), dtype=torch.uint8, device=dev)
             for label, act, r in (("identity_us", "identity", None), ("relu_us", "relu", None),
-                                  ("silu_residual_us", "silu", res)):
+                                  ("silu_residual_us", "silu", res), ("silu_fp8_out_us", "silu", "fp8")):
                 evs = []
                 for i in range(iters):
                     lb = sets[i % ROTATION][n]
@@ -516,15 +518,19 @@ def epilogue_variants(capi, sets, layers, stream, dev, iters, silu_us) -> dict:
                     a = torch.cuda.Event(enable_timing=True)
                     b = torch.cuda.Event(enable_timing=True)
                     a.record(stream)
-                    capi.forward_act(lb.x, lb.w, lb.scale, lb.bias, sh.stride, sh.pad, activation=act,
-                                     residual=r, y=lb.y, stream=stream)
+                    if isinstance(r, str):
+                        capi.forward_act_fp8(lb.x, lb.w, lb.scale, lb.bias, sh.stride, sh.pad, activation=act,
+                                             y=y8, stream=stream)
+                    else:
+                        capi.forward_act(lb.x, lb.w, lb.scale, lb.bias, sh.stride, sh.pad, activation=act,
+                                         residual=r, y=lb.y, stream=stream)
                     b.record(stream)
                     evs.append((a, b))
                 torch.cuda.synchronize()
                 capi.check(stream)
                 row[label] = round(1e3 * statistics.median(a.elapsed_time(b) for a, b in evs), 3)
             out[n] = row
-            del res
+            del res, y8
     del flush
     return {"layers": out, "timing": "median of isolated calls, L2 flushed before each",
             "residual_bytes_note": "the residual add reads one more bf16 tensor the size of y"}

@@ -80,6 +80,7 @@ _forward = _declare("conv_bn_silu_forward", [_p] * 5 + [_i] * 11 + [_p])
 _forward_algo = _declare("conv_bn_silu_forward_algo", [_p] * 5 + [_i] * 12 + [_p])
 _forward_noalloc = _declare("conv_bn_silu_forward_noalloc", [_p] * 5 + [_i] * 11 + [_p])
 _forward_act = _declare("conv_bn_act_forward", [_p] * 6 + [_i] * 12 + [_p])
+_forward_act_fp8 = _declare("conv_bn_act_forward_fp8", [_p] * 5 + [_i] * 12 + [_p])
 _forward_unfused = _declare("conv_bn_silu_forward_unfused", [_p] * 7 + [_i] * 11 + [_p])
 _bn_apply = _declare("conv_bn_silu_bn_apply", [_p] * 4 + [ctypes.c_longlong, _i, _p])
 _silu_apply = _declare("conv_bn_silu_silu_apply", [_p, _p, ctypes.c_longlong, _p])
@@ -307,6 +308,35 @@ def forward_act(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor, bias: tor
                       pres, _dev_tensor(y, torch.bfloat16, "y"), n, h, wi, c, c_out, r, s, sh, sw, ph, pw,
                       ACTIVATIONS[activation], _stream_handle(stream))
     _raise_if(st, "conv_bn_act_forward")
+    return y
+
+
+def forward_act_fp8(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor, bias: torch.Tensor,
+                    stride=1, pad=0, activation: str = "silu", y: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """conv_bn_act_forward_fp8: y = act(conv2d(x, w) * scale + bias) as fp8 e4m3 bytes (torch.uint8,
+    NHWC), each value rounded once to nearest even and saturated to +-448."""
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(ACTIVATIONS)}")
+    n, h, wi, c = x.shape
+    c_out, r, s, c2 = w.shape
+    if c2 != c:
+        raise ValueError(f"channel mismatch: x has {c}, w has {c2}")
+    sh, sw = _pair(stride)
+    ph, pw = _pair(pad)
+    ho, wo = output_dims(h, wi, r, s, (sh, sw), (ph, pw))
+    shape = (n, ho, wo, c_out)
+    if y is None:
+        y = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    elif tuple(y.shape) != shape:
+        raise ValueError(f"y has shape {tuple(y.shape)}, expected {shape}")
+    if y.numel() == 0:
+        return y
+    st = _forward_act_fp8(_dev_tensor(x, torch.bfloat16, "x"), _dev_tensor(w, torch.bfloat16, "w"),
+                          _dev_tensor(scale, torch.float32, "scale"), _dev_tensor(bias, torch.float32, "bias"),
+                          _dev_tensor(y, torch.uint8, "y"), n, h, wi, c, c_out, r, s, sh, sw, ph, pw,
+                          ACTIVATIONS[activation], _stream_handle(stream))
+    _raise_if(st, "conv_bn_act_forward_fp8")
     return y
 
 

@@ -119,7 +119,7 @@ int launch_forward(const cbs::ConvProblem &p, int algo, cudaStream_t strm, const
         cudaError_t e = cbs::tc_launch(p, plan, strm);
         return e == cudaSuccess ? CBS_OK : cuda_fail(e);
     }
-    if (has_overrides(rq)) return CBS_ERR_UNSUPPORTED;
+    if (has_overrides(rq) && !p.out_fp8) return CBS_ERR_UNSUPPORTED;
     cudaError_t e = cbs::direct_launch(p, strm);
     return e == cudaSuccess ? CBS_OK : cuda_fail(e);
 }
@@ -301,6 +301,36 @@ int conv_bn_act_forward(const void *x, const void *w, const float *scale, const 
     p.epi_mode = mode;
     p.residual = residual;
     return launch_forward(p, CBS_ALGO_AUTO, static_cast<cudaStream_t>(stream));
+}
+
+int conv_bn_act_forward_fp8(const void *x, const void *w, const float *scale, const float *bias, void *y,
+                            int n, int h, int w_in, int c, int c_out, int r, int s, int stride_h, int stride_w,
+                            int pad_h, int pad_w, int activation, void *stream)
+{
+    int mode;
+    switch (activation) {
+    case CBS_ACT_SILU: mode = cbs::kEpiSilu; break;
+    case CBS_ACT_IDENTITY: mode = cbs::kEpiBn; break;
+    case CBS_ACT_RELU: mode = cbs::kEpiRelu; break;
+    default: return CBS_ERR_INVALID_ARG;
+    }
+    cbs::ConvProblem p{};
+    int st = make_problem(n, h, w_in, c, c_out, r, s, stride_h, stride_w, pad_h, pad_w, &p);
+    if (st != CBS_OK) return st;
+    if (p.m == 0 || c_out == 0) return CBS_OK;
+    if (!x || !w || !scale || !bias || !y) return CBS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(scale) || !aligned16(bias) || !aligned16(y))
+        return CBS_ERR_MISALIGNED;
+    p.x = x;
+    p.w = w;
+    p.scale = scale;
+    p.bias = bias;
+    p.y = y;
+    p.epi_mode = mode;
+    p.out_fp8 = 1;
+    // Pixel-major tiles only: the channel-major (swap AB) epilogue writes bf16.
+    const cbs::PlanRequest rq{0, -1, -1, 0};
+    return launch_forward(p, CBS_ALGO_AUTO, static_cast<cudaStream_t>(stream), &rq);
 }
 
 int conv_bn_silu_forward_unfused(const void *x, const void *w, const float *scale, const float *bias,

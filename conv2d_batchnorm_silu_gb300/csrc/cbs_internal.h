@@ -30,6 +30,7 @@ struct ConvProblem {
     int epi_mode;          // EpiMode: SiLU (the layer), conv only, BN only, BN + ReLU
     const void *residual;  // nullable bf16 NHWC [m][c_out], added after the activation
     long long wait_timeout_ns;  // > 0: bound on the tcgen05 kernel's pipeline waits (0: the 2 s default)
+    int out_fp8;                // 1: y is fp8 e4m3 (one byte per element, round to nearest even, saturating)
 };
 
 // Tile configuration of the tcgen05 implicit GEMM.

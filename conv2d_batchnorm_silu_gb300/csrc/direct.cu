@@ -34,12 +34,22 @@ struct DirectArgs {
     int stride_h, stride_w, pad_h, pad_w, ho, wo;
     int epi_mode;   // EpiMode applied to the accumulator
     const __nv_bfloat16 *residual;  // nullable: bf16 [m][c_out] added after the activation
+    int out_fp8;    // 1: y holds fp8 e4m3 bytes
 };
 
 // Epilogue on the registers: BN multiply/add, activation, optional residual,
 // bf16, 16-byte stores when the channel run allows.
 __device__ __forceinline__ void store_outputs(const DirectArgs &a, long long m, int k0, const float *acc)
 {
+    if (a.out_fp8) {
+        unsigned char *y8 = reinterpret_cast<unsigned char *>(a.y) + m * a.c_out + k0;
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+            if (k0 + j < a.c_out)
+                y8[j] = dev::to_e4m3(dev::epilogue_value(acc[j], __ldg(a.scale + k0 + j), __ldg(a.bias + k0 + j),
+                                                         a.epi_mode));
+        return;
+    }
     __nv_bfloat16 *yp = a.y + m * a.c_out + k0;
     const __nv_bfloat16 *rp = a.residual != nullptr ? a.residual + m * a.c_out + k0 : nullptr;
     if (k0 + KB <= a.c_out && (a.c_out % 8) == 0) {
@@ -259,6 +269,7 @@ cudaError_t direct_launch(const ConvProblem &p, cudaStream_t stream)
     a.wo = p.wo;
     a.epi_mode = p.epi_mode;
     a.residual = static_cast<const __nv_bfloat16 *>(p.residual);
+    a.out_fp8 = p.out_fp8;
     cudaError_t err = cudaSuccess;
     if (try_small<3, 3, 1>(p, a, stream, &err) || try_small<3, 3, 3>(p, a, stream, &err) ||
         try_small<3, 3, 4>(p, a, stream, &err) || try_small<3, 3, 8>(p, a, stream, &err) ||

@@ -59,6 +59,23 @@ __device__ __forceinline__ float epilogue_from_half(float acc, float half_scale,
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
+// Four floats -> four fp8 e4m3 bytes (round to nearest even, saturating to +-448),
+// v0 in the lowest byte (the lowest address).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float v0, float v1, float v2, float v3)
+{
+    unsigned short lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(v1), "f"(v0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(v3), "f"(v2));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__device__ __forceinline__ unsigned char to_e4m3(float v)
+{
+    unsigned short two;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(two) : "f"(0.0f), "f"(v));
+    return (unsigned char)(two & 0xffu);
+}
+
 // Eight consecutive bf16 values of a residual tensor (16-byte aligned), added
 // to v[0..7] after the activation.
 __device__ __forceinline__ void add_residual8(float *v, const void *src)

@@ -237,6 +237,7 @@ __device__ __forceinline__ uint32_t swizzle_offset(uint32_t off)
 constexpr int kEpiKindSilu = 0;
 constexpr int kEpiKindMode = 1;
 constexpr int kEpiKindResidual = 2;
+constexpr int kEpiKindFp8 = 3;  // the launch's EpiMode with an fp8 e4m3 output (pixel-major tiles only)
 
 __device__ __forceinline__ void prefetch_l2(const void *p)
 {
@@ -251,6 +252,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 {
     static_assert(!(SWAP && PAIR), "CTA pairs serve the pixel-major (unswapped) tile only");
     constexpr bool RES = EPI == kEpiKindResidual;
+    constexpr bool FP8 = EPI == kEpiKindFp8;
+    static_assert(!(FP8 && SWAP), "the fp8 output is written by the pixel-major epilogue");
     // The epilogue mode: a compile-time constant for the fused layer.
     const int emode = EPI == kEpiKindSilu ? (int)kEpiSilu : a.epi_mode;
     constexpr int CG = PAIR ? 2 : 1;  // tcgen05 CTA group
@@ -675,7 +678,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 const int ch0 = n0 + col_base + j * EC;
                 uint32_t packed[EC / 2];
-                if constexpr (RES) {
+                uint32_t q8[FP8 ? EC / 4 : 1];
+                if constexpr (FP8) {
+                    // fp8 output: each value rounded once, from fp32 straight to e4m3.
+#pragma unroll
+                    for (int i = 0; i < EC; i += 4) {
+                        float f[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = ch0 + i + e;
+                            f[e] = c < a.c_out ? dev::epilogue_value(__uint_as_float(v[i + e]), __ldg(a.scale + c),
+                                                                     __ldg(a.bias + c), emode)
+                                               : 0.f;
+                        }
+                        q8[i / 4] = dev::pack_e4m3x4(f[0], f[1], f[2], f[3]);
+                    }
+                } else if constexpr (RES) {
                     // With a residual: this lane's pixel row, channels ch0.. (8 per 16-byte
                     // load; c_out % 8 == 0, so a group of 8 is wholly inside or outside).
                     const int pix = row0 + lane;
@@ -731,11 +749,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0) dev::bulk_wait_group_read<1>();
                 __syncwarp();
                 uint8_t *sb = my_stg + sbuf * C::STG_BYTES;
+                if constexpr (FP8) {
+                    // One byte per value: rows of EC bytes (32: 32-byte swizzle; 16: none).
+#pragma unroll
+                    for (int q = 0; q < EC / 16; ++q) {
+                        const uint32_t raw = (uint32_t)(lane * EC + q * 16);
+                        const uint32_t off = EC == 32 ? swizzle_offset<32>(raw) : raw;
+                        *reinterpret_cast<uint4 *>(sb + off) = make_uint4(q8[4 * q], q8[4 * q + 1], q8[4 * q + 2],
+                                                                          q8[4 * q + 3]);
+                    }
+                } else {
 #pragma unroll
                 for (int q = 0; q < ROW_Y / 16; ++q) {
                     const uint32_t off = swizzle_offset<ROW_Y>((uint32_t)(lane * ROW_Y + q * 16));
                     *reinterpret_cast<uint4 *>(sb + off) =
                         make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                }
                 }
                 dev::fence_proxy_async_shared();
                 __syncwarp();
@@ -847,6 +876,21 @@ cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swa
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     // y: (C_out, M), box (EC, 32): one epilogue warp's rows, one column chunk.
+    if (p.out_fp8) {
+        // fp8 e4m3 output, one byte per element: rows of EC bytes.
+        int split = 1, ec = 16;
+        tc_epilogue_geometry(block_n, &split, &ec);
+        cuuint64_t dims[2] = {(cuuint64_t)p.c_out, (cuuint64_t)p.m};
+        cuuint64_t strides[1] = {(cuuint64_t)p.c_out};
+        cuuint32_t box[2] = {(cuuint32_t)ec, 32};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = g_encode_tiled(&maps->y, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.y, dims, strides, box, estr,
+                                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                    ec == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        return cudaSuccess;
+    }
     {
         int split = 1, ec = 16;
         tc_epilogue_geometry(block_n, &split, &ec);
@@ -869,11 +913,11 @@ cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swa
 struct MapKey {
     const void *x, *w, *y;
     int dims[11];
-    int block_n, block_k, device, swap, pair;
+    int block_n, block_k, device, swap, pair, fp8;
     bool operator==(const MapKey &o) const
     {
         if (x != o.x || w != o.w || y != o.y || block_n != o.block_n || block_k != o.block_k ||
-            device != o.device || swap != o.swap || pair != o.pair)
+            device != o.device || swap != o.swap || pair != o.pair || fp8 != o.fp8)
             return false;
         for (int i = 0; i < 11; ++i)
             if (dims[i] != o.dims[i]) return false;
@@ -904,6 +948,7 @@ cudaError_t cached_maps(const ConvProblem &p, int block_n, int block_k, bool swa
     k.block_k = block_k;
     k.swap = swap ? 1 : 0;
     k.pair = pair ? 1 : 0;
+    k.fp8 = p.out_fp8;
     cudaError_t st = cudaGetDevice(&k.device);
     if (st != cudaSuccess) return st;
     {
@@ -1064,6 +1109,7 @@ bool tc_supported(const ConvProblem &p)
     // one K step must be one swizzle span of 32/64/128 bytes (c % 16).  The
     // im2col box corners are limited to [-128, 127]; the GEMM row count to int.
     if (p.c % 16 != 0 || p.c_out % 8 != 0) return false;
+    if (p.out_fp8 && p.c_out % 16 != 0) return false;  // 16-byte rows of one-byte outputs
     // Square filters with equal stride and padding on both axes only, so the
     // im2col box corners are the same along W and H.
     if (p.r != p.s || p.stride_h != p.stride_w || p.pad_h != p.pad_w) return false;
@@ -1207,11 +1253,15 @@ cudaError_t dispatch(const ConvProblem &p, const TcPlan &plan, const TcMaps &map
                      void *workspace)
 {
     if (plan.swap_ab) {
+        if constexpr (EPI == kEpiKindFp8) {
+            return cudaErrorInvalidConfiguration;  // the fp8 output is pixel-major only
+        } else {
         if (plan.block_n != 256) return cudaErrorInvalidConfiguration;
         if (plan.block_k == 64) return launch_cfg<256, 64, true, false, EPI>(p, plan, maps, stream, workspace);
         if (plan.block_k == 32) return launch_cfg<256, 32, true, false, EPI>(p, plan, maps, stream, workspace);
         if (plan.block_k == 16) return launch_cfg<256, 16, true, false, EPI>(p, plan, maps, stream, workspace);
         return cudaErrorInvalidConfiguration;
+        }
     }
     if (plan.pair) {
         if (plan.block_n != 256) return cudaErrorInvalidConfiguration;
@@ -1240,6 +1290,10 @@ cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, c
     TcMaps maps;
     cudaError_t st = cached_maps(p, plan.block_n, plan.block_k, plan.swap_ab != 0, plan.pair != 0, &maps);
     if (st != cudaSuccess) return st;
+    if (p.out_fp8) {
+        if (p.residual != nullptr || plan.swap_ab) return cudaErrorInvalidConfiguration;
+        return dispatch<kEpiKindFp8>(p, plan, maps, stream, workspace);
+    }
     if (p.residual != nullptr) return dispatch<kEpiKindResidual>(p, plan, maps, stream, workspace);
     if (p.epi_mode != kEpiSilu) return dispatch<kEpiKindMode>(p, plan, maps, stream, workspace);
     return dispatch<kEpiKindSilu>(p, plan, maps, stream, workspace);

@@ -389,6 +389,7 @@ bool try_gather(const ConvProblem &p, int sm_count, cudaStream_t stream, cudaErr
 bool gather_supported(const ConvProblem &p)
 {
     if (p.m > 0x7fffffffLL - 128) return false;
+    if (p.out_fp8) return false;  // the bf16 output only (the direct kernel writes fp8)
     const bool shape = p.r == 3 && p.s == 3 && (p.c == 1 || p.c == 3 || p.c == 4);
     return shape && p.c_out >= 1 && p.c_out <= 64;
 }

@@ -167,6 +167,20 @@ int conv_bn_act_forward(const void *x, const void *w, const float *scale, const 
                         void *stream);
 
 /*
+ * conv_bn_act_forward with a narrower output: y is fp8 e4m3 (1 sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits; largest finite value 448, no infinities),
+ * one byte per element, NHWC [n][ho][wo][c_out].  Each value is rounded once,
+ * from the fp32 epilogue result to the nearest e4m3 (ties to even), saturating
+ * to +-448 ("Fusing an Epilogue", section "What an epilogue is": casts to a
+ * narrower dtype are epilogue work).  No residual.  The tensor-core path needs
+ * c_out % 16 == 0 (16-byte rows) and uses pixel-major tiles; other shapes run
+ * on the direct kernel.
+ */
+int conv_bn_act_forward_fp8(const void *x, const void *w, const float *scale, const float *bias, void *y,
+                            int n, int h, int w_in, int c, int c_out, int r, int s, int stride_h, int stride_w,
+                            int pad_h, int pad_w, int activation, void *stream);
+
+/*
  * Unfused comparator: the same layer as the three-kernel sequence that the
  * fusion replaces -- the convolution writes t1 to memory, a BatchNorm kernel
  * reads t1 and writes t2, a SiLU kernel reads t2 and writes y ("Fusing an

@@ -262,3 +262,36 @@ def conv_bn_act_at(x_bits, w_bits, gamma, beta, mean, var, eps, pixels, stride=1
         res = bf16_bits_to_f64(residual_bits).reshape(-1, k)[np.asarray(pixels)]
     return bn_act(conv2d_at(x_bits, w_bits, pixels, stride, pad, threads), scale, bias, activation, res)
 
+
+# ---------------------------------------------------------------- fp8 e4m3 output
+E4M3_MAX = 448.0
+
+
+def e4m3_bits_to_f64(bits) -> np.ndarray:
+    """Decode fp8 e4m3 bytes: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0
+    holds the subnormals m * 2^-9; 0x7f / 0xff are NaN (no infinities)."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def to_e4m3_bits(values) -> np.ndarray:
+    """Round float64 values to the nearest fp8 e4m3 (ties to the even mantissa), saturating
+    to +-448: the narrower cast of the epilogue page's candidate list.  Written from the
+    format: the representable magnitudes are enumerated and the nearest one taken."""
+    v = np.asarray(values, dtype=np.float64)
+    codes = np.arange(0x7F, dtype=np.uint8)                  # every non-negative finite code
+    mags = e4m3_bits_to_f64(codes)                           # increasing with the code
+    a = np.minimum(np.abs(v), E4M3_MAX)
+    hi = np.clip(np.searchsorted(mags, a, side="left"), 0, len(mags) - 1)
+    lo = np.clip(hi - 1, 0, len(mags) - 1)
+    d_lo, d_hi = a - mags[lo], mags[hi] - a
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (codes[hi] % 2 == 0) & (hi != lo))
+    code = np.where(take_hi, codes[hi], codes[lo]).astype(np.uint8)
+    code = np.where(a == mags[hi], codes[hi], code).astype(np.uint8)
+    return (code | np.where(np.signbit(v), 0x80, 0).astype(np.uint8)).astype(np.uint8)
+

@@ -154,6 +154,10 @@ def test_invalid_arguments_return_status_without_gpu(lib):
     assert f(act, good, good, good, good, good, None, *dims, 1, None) == lib.CBS_ERR_INVALID_ARG
     assert f(act, None, None, None, None, None, None, 0, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1, 0,
              None) == lib.CBS_OK
+    # fp8 output: bad activation id, misaligned output
+    f8 = "conv_bn_act_forward_fp8"
+    assert f(f8, good, good, good, good, good, *dims, 3, None) == lib.CBS_ERR_INVALID_ARG
+    assert f(f8, good, good, good, good, odd, *dims, 0, None) == lib.CBS_ERR_MISALIGNED
     # batched fold: every layer validated before any launch
     FL = lib.FoldLayer
     ok_layer = FL(0x10000, 0x10000, 0x10000, 0x10000, 1e-3, 4, 0x10000, 0x10000)

@@ -53,6 +53,8 @@ PY_MUTANTS = {
                             "        y = y + np.asarray(residual, dtype=np.float64)",
                             "z = bn(conv, scale, bias)\n    if residual is not None:\n"
                             "        z = z + np.asarray(residual, dtype=np.float64)\n    y = activate(z, activation)"),
+    "e4m3_ties_up": ("(codes[hi] % 2 == 0) & (hi != lo)", "(hi != lo)"),
+    "e4m3_sign_dropped": ("np.where(np.signbit(v), 0x80, 0)", "np.where(np.signbit(v), 0, 0)"),
 }
 
 
@@ -153,7 +155,11 @@ def py_pins_pass(mod):
         z = conv[0, k] * s + b
         if abs(got[0, k] - float(mpmath.mpf(z) / (1 + mpmath.exp(-mpmath.mpf(z))))) > 1e-14:
             return False
-    return epilogue_pins_pass(mod)
+    if not epilogue_pins_pass(mod):
+        return False
+    # fp8 e4m3 cast: a tie to even, a tie below, saturation (hand-derived in test_oracle_fp8.py)
+    e = mod.to_e4m3_bits(np.array([1.0625, 17.0, 232.0, 1000.0, -1e30]))
+    return [int(c) for c in e] == [0x38, 0x58, 0x76, 0x7E, 0xFE]
 
 
 def epilogue_pins_pass(mod):
