@@ -18,8 +18,9 @@ reads its data from HBM.  The step is replayed from CUDA graphs captured
 from the API calls (six launches through Python per step would make the host
 the bottleneck); the dominant layer's forward is its own graph, so CUDA events
 on the stream bracket exactly that kernel inside the timed region.  Per-layer
-times in ``per_layer`` come from a separate pass with the L2 flushed before
-each call.  SM clocks and throttle reasons are sampled with nvidia-smi during
+times in ``per_layer`` come from two separate passes: each call alone with the
+L2 flushed before it, and each layer's forward back to back in a CUDA graph
+over enough buffer sets that their rotation exceeds the L2.  SM clocks and throttle reasons are sampled with nvidia-smi during
 the timed region.
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead
@@ -81,6 +82,10 @@ def parse_args(argv=None):
                     help="skip the fused-vs-unfused comparison (conv, BN and SiLU as three kernels)")
     ap.add_argument("--no-epilogues", action="store_true",
                     help="skip the per-layer timing of the other epilogues (identity, ReLU, residual add)")
+    ap.add_argument("--b2b-replays", type=int, default=20,
+                    help="graph replays for the back-to-back per-layer times (0: skip)")
+    ap.add_argument("--no-gemm-context", action="store_true",
+                    help="skip timing cuBLAS on plain GEMMs of the pointwise and deep layers' sizes")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch through the API each step instead of replaying CUDA graphs")
     args = ap.parse_args(argv)
@@ -359,6 +364,8 @@ def run_ours(args, rank, world, local_rank):
     dom_us = 1e3 * float(np.mean([a.elapsed_time(b) for a, b in zip(*dom_ev)]))
 
     peaks, peak_src = load_peaks()
+    b2b = layer_times_back_to_back(capi, sets, inputs, layers, stream, dev,
+                                   args.b2b_replays) if args.b2b_replays > 0 else None
     iso = isolated_layer_times(capi, sets, layers, stream, dev, args.iso_iters)
     per_layer = {}
     for n in layers:
@@ -375,6 +382,12 @@ def run_ours(args, rank, world, local_rank):
                         "bound": "tensor" if t_flop >= t_byte else "hbm",
                         "kernel": pl["algo"], "tile": [pl["block_m"], pl["block_n"], pl["block_k"]],
                         "grid": pl["grid"]}
+        if b2b is not None:
+            tb = b2b[n]["us"] * 1e-6
+            per_layer[n]["us_back_to_back"] = round(b2b[n]["us"], 3)
+            per_layer[n]["roofline_frac_back_to_back"] = round(max(t_flop, t_byte) / tb, 4)
+            if b2b[n]["l2_resident"]:
+                per_layer[n]["back_to_back_l2_resident"] = True
     dom = LAYERS[dominant]
     dom_t = dom_us * 1e-6
     if per_layer[dominant]["bound"] == "tensor":
@@ -395,6 +408,8 @@ def run_ours(args, rank, world, local_rank):
 
     epilogues = None if args.no_epilogues else \
         epilogue_variants(capi, sets, layers, stream, dev, args.iso_iters, iso)
+
+    gemm = None if args.no_gemm_context else gemm_context(dev, layers, iso, args.iso_iters)
 
     e2e = run_e2e(args, capi, inputs, dev, stream, world) if args.e2e_steps > 0 else None
     cpu = None
@@ -418,6 +433,15 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world} (each rank runs the full step)"},
         "roofline": roofline,
         "per_layer": per_layer,
+        "per_layer_timing": {
+            "us_per_call": "median of isolated calls, a 512 MB L2-flushing write before each; "
+                           "includes the launch gap of a lone call",
+            "us_back_to_back": (None if b2b is None else
+                                "one CUDA graph of G forwards of the layer back to back, each on its own "
+                                "buffer set (rotation > 160 MB unless marked l2_resident), replayed "
+                                f"{args.b2b_replays} times; graph time / (replays x G)"),
+            "back_to_back_sets": None if b2b is None else {n: b2b[n]["calls_per_graph"] for n in b2b}},
+        "gemm_context": gemm,
         "fusion": fusion,
         "epilogues": epilogues,
         "cpu_baseline": cpu,
@@ -429,6 +453,83 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(world)
+
+
+def layer_times_back_to_back(capi, sets, inputs, layers, stream, dev, replays) -> dict:
+    """Steady-state time per call of each layer: one CUDA graph of G forwards of the layer
+    back to back, each on its own buffer set, replayed; time per call = graph time / G.
+    Consecutive forwards overlap their launch and prologue with the previous one's tail
+    (programmatic dependent launch), as layers do inside a network.  G is chosen so that
+    the sets rotate through more than 160 MB (more than the 129 MB L2); a layer too small
+    for that within 64 sets is reported with "l2_resident": true."""
+    out = {}
+    for n in layers:
+        sh = LAYERS[n]
+        g_sets = max(ROTATION, -(-160_000_000 // sh.compulsory_bytes))
+        resident = g_sets > 64
+        g_sets = min(g_sets, 64)
+        bufs = [sets[i][n] for i in range(ROTATION)] + \
+               [LayerBuffers(inputs[n], dev) for _ in range(g_sets - ROTATION)]
+        with torch.cuda.stream(stream):
+            for lb in bufs[ROTATION:]:
+                capi.fold(lb.g, lb.b, lb.m, lb.v, lb.eps, scale=lb.scale, bias=lb.bias, stream=stream)
+                capi.forward(lb.x, lb.w, lb.scale, lb.bias, sh.stride, sh.pad, y=lb.y, stream=stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for lb in bufs:
+                capi.forward(lb.x, lb.w, lb.scale, lb.bias, sh.stride, sh.pad, y=lb.y)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(replays):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        capi.check(stream)
+        out[n] = {"us": 1e3 * e0.elapsed_time(e1) / (replays * g_sets), "calls_per_graph": g_sets,
+                  "rotation_mb": round(g_sets * sh.compulsory_bytes / 1e6, 1), "l2_resident": resident}
+        del g, bufs
+    return out
+
+
+def gemm_context(dev, layers, fused_us, iters) -> dict:
+    """Context, not part of the step: cuBLAS (torch.matmul, bf16) on a plain GEMM of the
+    same M, N and K as a layer -- the pointwise layer is exactly that GEMM plus the
+    epilogue; for a 3x3 layer the GEMM skips the implicit im2col.  Timed like the
+    per-layer forwards (L2 flushed before each call, median)."""
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    out = {}
+    for n in ("pointwise", "deep"):
+        if n not in layers:
+            continue
+        sh = LAYERS[n]
+        m, k, c = sh.m, sh.k, sh.c * sh.r * sh.s
+        a = torch.randn(m, c, device=dev).to(torch.bfloat16)
+        b = torch.randn(c, k, device=dev).to(torch.bfloat16)
+        for _ in range(3):
+            a @ b
+        evs = []
+        for _ in range(iters):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            a @ b
+            e1.record()
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        us = 1e3 * statistics.median(x.elapsed_time(y) for x, y in evs)
+        out[n] = {"gemm": f"{m}x{k}x{c} (M x N x K)", "cublas_us": round(us, 3),
+                  "cublas_tflops": round(2 * m * k * c / us / 1e6, 1),
+                  "fused_conv_us": round(fused_us[n], 3),
+                  "fused_over_cublas": round(fused_us[n] / us, 3)}
+        del a, b
+    del flush
+    return {"layers": out, "note": "cuBLAS on the same-size plain GEMM without BN/SiLU; context only"}
 
 
 def isolated_layer_times(capi, sets, layers, stream, dev, iters) -> dict:

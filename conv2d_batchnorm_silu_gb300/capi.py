@@ -42,7 +42,8 @@ _f = ctypes.c_float
 class PlanInfo(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in (
         "algo", "block_m", "block_n", "block_k", "stages", "tiles", "grid", "threads",
-        "smem_bytes", "k_iters", "stream_k", "swap_ab", "cluster")] + [("workspace_bytes", ctypes.c_longlong)]
+        "smem_bytes", "k_iters", "stream_k", "swap_ab", "cluster")] + [("workspace_bytes", ctypes.c_longlong),
+                                                                        ("balanced", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         d = {name: getattr(self, name) for name, _ in self._fields_}
@@ -60,11 +61,13 @@ class PlanRequest(ctypes.Structure):
     """cbs_plan_request: overrides of the planner's choices (-1 / 0: planner's choice) and the
     bound on the tcgen05 kernel's pipeline waits (0: the 2 s default)."""
     _fields_ = [(name, ctypes.c_int) for name in ("algo", "swap_ab", "stream_k", "pair", "block_n")] + \
-        [("wait_timeout_ns", ctypes.c_longlong)]
+        [("wait_timeout_ns", ctypes.c_longlong), ("balanced", ctypes.c_int)]
 
 
-def _request(algo="auto", swap_ab=-1, stream_k=-1, pair=-1, block_n=0, wait_timeout_ns=0) -> PlanRequest:
-    return PlanRequest(ALGOS[algo], int(swap_ab), int(stream_k), int(pair), int(block_n), int(wait_timeout_ns))
+def _request(algo="auto", swap_ab=-1, stream_k=-1, pair=-1, block_n=0, wait_timeout_ns=0,
+             balanced=-1) -> PlanRequest:
+    return PlanRequest(ALGOS[algo], int(swap_ab), int(stream_k), int(pair), int(block_n), int(wait_timeout_ns),
+                       int(balanced))
 
 
 def _declare(name, argtypes, restype=ctypes.c_int):
@@ -155,7 +158,8 @@ def plan(n, h, w, c, c_out, r, s, stride=1, pad=0, algo="auto", sm_count: int = 
 
 
 def plan_request(n, h, w, c, c_out, r, s, stride=1, pad=0, sm_count: int = 152, **overrides) -> dict:
-    """conv_bn_silu_plan_request: the plan with overrides (algo, swap_ab, stream_k, pair, block_n)."""
+    """conv_bn_silu_plan_request: the plan with overrides (algo, swap_ab, stream_k, pair, block_n,
+    balanced)."""
     sh, sw = _pair(stride)
     ph, pw = _pair(pad)
     req = _request(**overrides)

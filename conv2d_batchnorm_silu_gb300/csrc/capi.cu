@@ -97,7 +97,8 @@ int sm_count_current_device(int *count)
 // A request's tcgen05 overrides, or nullptr when it leaves every choice to the planner.
 bool has_overrides(const cbs::PlanRequest *rq)
 {
-    return rq && (rq->swap_ab >= 0 || rq->stream_k >= 0 || rq->pair >= 0 || rq->block_n != 0);
+    return rq && (rq->swap_ab >= 0 || rq->stream_k >= 0 || rq->pair >= 0 || rq->block_n != 0 ||
+                  rq->balanced >= 0);
 }
 
 // Validated problem (pointers set) -> the chosen kernel's launch on `strm`.
@@ -130,13 +131,13 @@ int read_request(const cbs_plan_request *req, int *algo, cbs::PlanRequest *rq)
     if (!req) return CBS_ERR_INVALID_ARG;
     if (req->wait_timeout_ns < 0) return CBS_ERR_INVALID_ARG;
     if (req->algo < CBS_ALGO_AUTO || req->algo > CBS_ALGO_DIRECT) return CBS_ERR_INVALID_ARG;
-    for (int v : {req->swap_ab, req->stream_k, req->pair})
+    for (int v : {req->swap_ab, req->stream_k, req->pair, req->balanced})
         if (v < -1 || v > 1) return CBS_ERR_INVALID_ARG;
     if (req->block_n != 0 && req->block_n != 16 && req->block_n != 32 && req->block_n != 64 &&
         req->block_n != 128 && req->block_n != 256)
         return CBS_ERR_INVALID_ARG;
     *algo = req->algo;
-    *rq = cbs::PlanRequest{req->swap_ab, req->stream_k, req->pair, req->block_n};
+    *rq = cbs::PlanRequest{req->swap_ab, req->stream_k, req->pair, req->block_n, req->balanced};
     return CBS_OK;
 }
 
@@ -329,7 +330,7 @@ int conv_bn_act_forward_fp8(const void *x, const void *w, const float *scale, co
     p.epi_mode = mode;
     p.out_fp8 = 1;
     // Pixel-major tiles only: the channel-major (swap AB) epilogue writes bf16.
-    const cbs::PlanRequest rq{0, -1, -1, 0};
+    const cbs::PlanRequest rq{0, -1, -1, 0, -1};
     return launch_forward(p, CBS_ALGO_AUTO, static_cast<cudaStream_t>(stream), &rq);
 }
 
@@ -439,6 +440,7 @@ static int fill_plan(const cbs::ConvProblem &p, int algo, int sm_count, const cb
         out.swap_ab = t.swap_ab;
         out.cluster = t.pair ? 2 : 1;
         out.workspace_bytes = t.workspace_bytes;
+        out.balanced = t.balanced;
     } else {
         if (has_overrides(rq)) return CBS_ERR_UNSUPPORTED;  // the direct kernel has no tilings to choose
         const long long bx = (p.m + cbs::kDirectThreads - 1) / cbs::kDirectThreads;

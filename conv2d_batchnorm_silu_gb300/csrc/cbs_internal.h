@@ -46,6 +46,7 @@ struct TcPlan {
     int swap_ab;                  // 1: tile = 128 channels x block_n pixels, D = W * X^T
     int pair;                     // 1: clusters of two CTAs run the 2-CTA MMA, each holding half the weight tile
     int stream_k;                 // 1: K steps split evenly over the grid (see tc_conv.cu)
+    int balanced;                 // swap_ab only: each CTA takes an equal run of 32-pixel chunks (see tc_conv.cu)
     long long workspace_bytes;    // stream-K partial tiles + flags (0 when not split)
     long long flag_bytes;         // the leading part of the workspace that must start zeroed
 };
@@ -105,6 +106,7 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count);
 // Overrides of the planner's tcgen05 choices: -1 (block_n: 0) leaves a choice to the planner.
 struct PlanRequest {
     int swap_ab, stream_k, pair, block_n;
+    int balanced;  // channel-major tiles: -1 planner, 0 whole 256-pixel tiles, 1 equal runs of 32-pixel chunks
 };
 // As tc_make_plan with the overrides in `rq` (nullable); -1 when the kernel cannot run
 // them on this shape (e.g. stream-K shares shorter than one tile).

@@ -58,11 +58,15 @@ struct TcArgs {
     unsigned long long wait_ns;  // bound on every pipeline wait (draining copies in flight keeps 2 s)
     float *partial;  // stream-K: [grid-1][128*BN] fp32 partial tiles (slot c: boundary of CTAs c, c+1)
     int *flags;      // stream-K: per slot, a ready flag and an arrival ticket per epilogue warp; 0 between launches
+    int balanced;    // swap AB: each CTA takes an equal run of 32-pixel chunks (see WorkIter)
+    int chunks_m;    // balanced: 32-pixel chunks per channel tile, ceil(m / 32)
 };
 
-// K steps [kb, ke) of output tile `tile`.
+// K steps [kb, ke) of output tile `tile`.  Balanced channel-major units: `tile`
+// is the channel tile and the unit covers pixels [p0, p0 + np).
 struct WorkUnit {
     int tile, kb, ke;
+    int p0, np;
 };
 
 // The units one worker processes.  A worker is a CTA, or a CTA pair sharing
@@ -81,12 +85,20 @@ struct WorkIter {
     int t_full, t_full_end;  // whole tiles [t_full, t_full_end)
     // data-parallel state
     int t, stride;
+    // balanced channel-major state: chunks [g, g1) of the (channel tile, 32-pixel chunk)
+    // sequence, channel tile major.
+    int g, g1;
     // vb / vg: this worker's index and the worker count (a CTA, or a CTA pair).
     __device__ WorkIter(const TcArgs &a, int vb, int vg)
     {
         state = 0;
         t = vb;
         stride = vg;
+        if (a.balanced) {
+            const long long total = (long long)a.n_tiles * a.chunks_m;
+            g = (int)(total * vb / vg);
+            g1 = (int)(total * (vb + 1) / vg);
+        }
         if (a.stream_k) {
             const long long total = (long long)a.tiles * a.k_iters;
             const long long g0 = total * vb / vg, g1 = total * (vb + 1) / vg;
@@ -107,6 +119,22 @@ struct WorkIter {
     // neighbouring workers, too) mid-kernel, and the last epilogue is a plain one.
     __device__ bool next(const TcArgs &a, WorkUnit &u)
     {
+        if (a.balanced) {
+            // Within one channel tile the worker's chunks are cut into units of 256
+            // pixels (two whole im2col boxes) and one shorter remainder, so that no
+            // box is loaded for fewer pixels than it holds except in the remainder.
+            if (g >= g1) return false;
+            const int nt = g / a.chunks_m;
+            const int piece_end = g1 < (nt + 1) * a.chunks_m ? g1 : (nt + 1) * a.chunks_m;
+            const int take = piece_end - g < 8 ? piece_end - g : 8;
+            u.tile = nt;
+            u.p0 = (g - nt * a.chunks_m) * 32;
+            u.np = a.m - u.p0 < take * 32 ? a.m - u.p0 : take * 32;
+            u.kb = 0;
+            u.ke = a.k_iters;
+            g += take;
+            return true;
+        }
         if (a.stream_k) {
             if (state == 0) {
                 state = 1;
@@ -251,6 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                            const __grid_constant__ CUtensorMap tm_y, const TcArgs a)
 {
     static_assert(!(SWAP && PAIR), "CTA pairs serve the pixel-major (unswapped) tile only");
+    static_assert(!SWAP || TcCfg<BN, BK>::EC == 32, "channel-major units are cut in 32-pixel chunks");
     constexpr bool RES = EPI == kEpiKindResidual;
     constexpr bool FP8 = EPI == kEpiKindFp8;
     static_assert(!(FP8 && SWAP), "the fp8 output is written by the pixel-major epilogue");
@@ -327,8 +356,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             while (!*abort_flag && wi.next(a, u)) {
                 const int m_unit = u.tile / a.n_tiles;
                 const int m_tile = PAIR ? 2 * m_unit + rank : m_unit;
-                const int n0 = (u.tile - m_unit * a.n_tiles) * (SWAP ? C::BM : BN);  // first channel
-                const int m0 = m_tile * (SWAP ? BN : C::BM);                        // first pixel
+                const bool bal = SWAP && a.balanced;
+                const int n0 = bal ? u.tile * C::BM : (u.tile - m_unit * a.n_tiles) * (SWAP ? C::BM : BN);
+                const int m0 = bal ? u.p0 : m_tile * (SWAP ? BN : C::BM);  // first pixel
+                // SWAP: one 128-pixel box, or two when the unit has more pixels than one holds.
+                const bool two_boxes = !bal || u.np > C::BM;
                 const int img = m0 / a.howo;
                 const int rem = m0 - img * a.howo;
                 const int oh = rem / a.wo;
@@ -366,14 +398,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         dev::tma_load_3d_pair(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f0, cc * BK,
                                               r * a.s + s, n0 + rank * (BN / 2));
                     } else if constexpr (SWAP) {
-                        dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES + C::B_BYTES);
+                        dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES + (two_boxes ? 2 : 1) * C::BM * BK * 2);
                         dev::tma_load_3d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_w, f_bar,
                                          cc * BK, r * a.s + s, n0);
                         const uint32_t bdst = dev::smem_u32(sm_b + stage * C::B_STRIDE);
                         dev::tma_load_im2col_4d(bdst, &tm_x, f_bar, cc * BK, corner_w, corner_h, img,
                                                 (uint16_t)s, (uint16_t)r);
-                        dev::tma_load_im2col_4d(bdst + C::BM * BK * 2, &tm_x, f_bar, cc * BK, corner_w1,
-                                                corner_h1, img1, (uint16_t)s, (uint16_t)r);
+                        if (two_boxes)
+                            dev::tma_load_im2col_4d(bdst + C::BM * BK * 2, &tm_x, f_bar, cc * BK, corner_w1,
+                                                    corner_h1, img1, (uint16_t)s, (uint16_t)r);
                     } else {
                         dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES + C::B_BYTES);
                         dev::tma_load_im2col_4d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_x, f_bar,
@@ -441,6 +474,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 dev::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                // Balanced channel-major units: the MMA's N is the unit's pixel count
+                // (rounded up to 16; the rows past it were loaded as zeros or neighbours
+                // and are never stored).
+                const uint32_t idesc_u =
+                    (SWAP && a.balanced) ? dev::idesc_bf16_f32(C::BM, (u.np + 15) & ~15) : idesc;
                 for (int it = u.kb; it < u.ke; ++it) {
                     if (!dev::mbar_wait_bounded(dev::smem_u32(&full[stage]), phase, abort_flag,
                                                 a.wait_ns)) {
@@ -451,10 +489,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     dev::tc_fence_after_sync();
                     const uint64_t da = desc_a0 + (uint64_t)(stage * (C::A_STRIDE >> 4));
                     const uint64_t db = desc_b0 + (uint64_t)(stage * (C::B_STRIDE >> 4));
-                    dev::tc_mma_bf16<CG>(d_tmem, da, db, idesc, it != u.kb ? 1u : 0u);
+                    dev::tc_mma_bf16<CG>(d_tmem, da, db, idesc_u, it != u.kb ? 1u : 0u);
 #pragma unroll
                     for (int kk = 1; kk < BK / 16; ++kk)
-                        dev::tc_mma_bf16<CG>(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc,
+                        dev::tc_mma_bf16<CG>(d_tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc_u,
                                              1u);
                     if constexpr (PAIR)
                         dev::tc_commit_multicast<CG>(dev::smem_u32(&empty[stage]), (uint16_t)0x3);
@@ -490,16 +528,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int row = ew * 32 + lane;  // this thread's row of the tile (TMEM lane)
         WorkIter wi(a, vb, vg);
         WorkUnit u;
+        // SWAP: a unit's channel tile, first pixel and count of EC-pixel chunks.  The
+        // two warps of a lane quarter take alternate chunks.
+        const int half = ep >> 2;
+        auto swap_geometry = [&](const WorkUnit &q, int &nt, int &p0, int &nchunks) {
+            if (a.balanced) {
+                nt = q.tile;
+                p0 = q.p0;
+                nchunks = (q.np + EC - 1) / EC;
+            } else {
+                const int pt = q.tile / a.n_tiles;
+                nt = q.tile - pt * a.n_tiles;
+                p0 = pt * BN;
+                nchunks = BN / EC;
+            }
+        };
         // Residual epilogue: bring a unit's residual rows (this warp's part) into L2
         // while its K loop runs, so that the epilogue's loads of them hit L2.
         auto prefetch_residual = [&](const WorkUnit &q) {
             if constexpr (RES) {
                 if constexpr (SWAP) {
-                    const int pt = q.tile / a.n_tiles;
-                    const int chw = (q.tile - pt * a.n_tiles) * C::BM + ew * 32;
+                    int nt, p0, nchunks;
+                    swap_geometry(q, nt, p0, nchunks);
+                    const int chw = nt * C::BM + ew * 32;
                     if (chw < a.c_out) {
-                        for (int i = 0; i < C::EPI_COLS / 32; ++i) {
-                            const int px = pt * BN + col_base + i * 32 + lane;
+                        for (int j = half; j < nchunks; j += C::SPLIT) {
+                            const int px = p0 + j * EC + lane;  // EC == 32 on this path
                             if (px < a.m) prefetch_l2(a.residual + (size_t)px * a.c_out + chw);
                         }
                     }
@@ -546,16 +600,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // channel, so BN scale/bias are per-thread constants; the tile is
                 // transposed to NHWC through shared memory, 32 pixels x 32 channels
                 // per TMA store.
-                const int p_tile = u.tile / a.n_tiles;
-                const int ch_w0 = (u.tile - p_tile * a.n_tiles) * C::BM + ew * 32;  // warp's first channel
+                int nt, p0, nchunks;
+                swap_geometry(u, nt, p0, nchunks);
+                const int ch_w0 = nt * C::BM + ew * 32;  // warp's first channel
                 const int ch = ch_w0 + lane;
                 const float hs = ch < a.c_out ? 0.5f * __ldg(a.scale + ch) : 0.f;
                 const float hb = ch < a.c_out ? 0.5f * __ldg(a.bias + ch) : 0.f;
-                const int px_base = p_tile * BN + col_base;
-                const uint32_t t_lane =
-                    tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN + col_base);
+                const uint32_t t_lane = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN);
+                if (half >= nchunks) {
+                    // A unit narrower than two chunks leaves this warp nothing to read.
+                    dev::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
+                }
 #pragma unroll 1
-                for (int j = 0; j < C::EPI_COLS / EC; ++j) {
+                for (int j = half; j < nchunks; j += C::SPLIT) {
                     uint32_t v[EC];
 #pragma unroll
                     for (int q = 0; q < EC / 16; ++q)
@@ -563,7 +622,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     dev::tmem_ld_wait();
 #pragma unroll
                     for (int q = 0; q < EC / 16; ++q) dev::reg_fence16(v + q * 16);
-                    if (j == C::EPI_COLS / EC - 1) {
+                    if (j + C::SPLIT >= nchunks) {
+                        // This warp's last chunk is in registers: release the accumulator.
                         dev::tc_fence_before_sync();
                         __syncwarp();
                         if (lane == 0) dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
@@ -571,7 +631,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) dev::bulk_wait_group_read<1>();
                     __syncwarp();
                     __nv_bfloat16 *sb = reinterpret_cast<__nv_bfloat16 *>(my_stg + sbuf * C::STG_BYTES);
-                    const int px0 = px_base + j * EC;
+                    const int px0 = p0 + j * EC;
                     if constexpr (RES) {
                         // Residual of this lane's channel for the chunk's pixels (across the
                         // warp, one 64-byte run of channels per pixel), all loaded first.
@@ -1066,6 +1126,8 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
     a.wait_ns = p.wait_timeout_ns > 0 ? (unsigned long long)p.wait_timeout_ns : kWaitTimeoutNs;
     a.partial = nullptr;
     a.flags = nullptr;
+    a.balanced = plan.swap_ab ? plan.balanced : 0;
+    a.chunks_m = (int)((p.m + 31) / 32);
     if (plan.stream_k) {
         void *ws = caller_workspace;
         if (ws == nullptr) {
@@ -1121,9 +1183,43 @@ bool tc_supported(const ConvProblem &p)
 
 static bool valid_block_n(int bn) { return bn == 16 || bn == 32 || bn == 64 || bn == 128 || bn == 256; }
 
+// Channel-major schedules: the most 128-pixel im2col boxes (per K step) that any
+// CTA loads.  Whole tiles: two per tile, tiles dealt round-robin.  Balanced: each
+// CTA's equal run of 32-pixel chunks, cut per channel tile into 256-pixel units
+// and one remainder (as the kernel's WorkIter cuts them).
+static long long swap_boxes_whole(long long tiles, int grid)
+{
+    return (tiles + grid - 1) / grid * 2;
+}
+
+static long long swap_boxes_balanced(long long m, int n_tiles, int grid)
+{
+    const long long cm = (m + 31) / 32, total = cm * n_tiles;
+    long long worst = 0;
+    for (int b = 0; b < grid; ++b) {
+        long long g = total * b / grid;
+        const long long g1 = total * (b + 1) / grid;
+        long long boxes = 0;
+        while (g < g1) {  // one channel tile's piece of the run per pass
+            const long long nt = g / cm;
+            const long long pe = std::min(g1, (nt + 1) * cm);
+            const long long len = pe - g;
+            boxes += len / 8 * 2;
+            if (len % 8) {
+                const long long p0 = (g + len / 8 * 8 - nt * cm) * 32;
+                const long long np = std::min(len % 8 * 32, m - p0);
+                boxes += np > kTcBlockM ? 2 : 1;
+            }
+            g = pe;
+        }
+        worst = std::max(worst, boxes);
+    }
+    return worst;
+}
+
 int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *rq, TcPlan *out)
 {
-    const PlanRequest dflt{-1, -1, -1, 0};
+    const PlanRequest dflt{-1, -1, -1, 0, -1};
     const PlanRequest &q = rq ? *rq : dflt;
     if (q.block_n != 0 && !valid_block_n(q.block_n)) return -1;
     TcPlan t{};
@@ -1169,14 +1265,30 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
                     : 0;
     if (q.swap_ab >= 0) t.swap_ab = q.swap_ab ? 1 : 0;
     if (t.swap_ab) {
-        // The channel-major tile is 128 channels x 256 pixels, whole tiles only.
+        // The channel-major tile is 128 channels x up to 256 pixels.  Whole 256-pixel
+        // tiles leave a partly idle last wave (the pointwise layer: 200 tiles on 152
+        // SMs); balanced, each CTA instead takes an equal run of the (channel tile,
+        // 32-pixel chunk) sequence, cut into units of at most 256 pixels.
         if ((q.block_n != 0 && q.block_n != 256) || q.stream_k == 1 || q.pair == 1) return -1;
         t.block_n = 256;
         t.stages = stages_for(256, t.block_k);
         t.m_tiles = (int)ptiles256;
         t.n_tiles = (p.c_out + kTcBlockM - 1) / kTcBlockM;
         t.tiles = t.m_tiles * t.n_tiles;
-        t.grid = std::min(t.tiles, sm_count);
+        // Balanced runs when they cut the busiest CTA's im2col boxes (the loads bound
+        // these layers) by a quarter or more: the pointwise layer's 200 tiles put four
+        // boxes per K step on 48 CTAs, equal runs at most three on any.  Smaller gains
+        // were within the noise of the measured sweep (tune module), and the shorter
+        // remainder units cost some of it back.
+        const long long chunks = (p.m + 31) / 32 * t.n_tiles;
+        const int grid_bal = (int)std::min<long long>(chunks, sm_count);
+        const int grid_whole = std::min(t.tiles, sm_count);
+        t.balanced = q.balanced >= 0 ? q.balanced
+                                     : (4 * swap_boxes_balanced(p.m, t.n_tiles, grid_bal) <=
+                                                3 * swap_boxes_whole(t.tiles, grid_whole)
+                                            ? 1
+                                            : 0);
+        t.grid = t.balanced ? grid_bal : grid_whole;
         t.smem_bytes = tc_smem_bytes(256, t.block_k, t.stages, 0);
         t.stream_k = 0;
         t.pair = 0;
@@ -1185,6 +1297,8 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
         *out = t;
         return 0;
     }
+    if (q.balanced == 1) return -1;  // balanced runs are a channel-major schedule
+    t.balanced = 0;
     if (q.block_n != 0) t.block_n = q.block_n;
     t.stages = stages_for(t.block_n, t.block_k);
     t.m_tiles = m_tiles;

@@ -7,7 +7,8 @@ down, with a bench whose job is to check they still hold.  This is that
 bench for this library: for each layer shape it times the planner's own
 choice ("auto"), the CUDA-core direct kernel, and each tcgen05 tiling the
 shape admits (pixel-major or channel-major tiles, whole tiles or stream-K,
-single CTAs or 2-CTA pairs, 128- or 256-wide tiles), each call alone with
+single CTAs or 2-CTA pairs, 128- or 256-wide tiles; channel-major tiles dealt
+whole or as equal runs of 32-pixel chunks), each call alone with
 the L2 flushed before it, and reports how far the planner's choice is from
 the fastest.
 
@@ -61,9 +62,14 @@ def variants():
             continue
         if pair and (not sk or bn != 256):
             continue
-        label = "swap" if swap else f"n{bn}{'-sk' if sk else ''}{'-pair' if pair else ''}"
-        yield label, {"algo": "tcgen05", "swap_ab": swap, "stream_k": sk, "pair": pair,
-                      "block_n": 0 if swap else bn}
+        if swap:
+            # channel-major: equal runs of 32-pixel chunks, or whole 256-pixel tiles
+            yield "swap", {"algo": "tcgen05", "swap_ab": 1, "stream_k": 0, "pair": 0, "block_n": 0, "balanced": 1}
+            yield "swap-tiles", {"algo": "tcgen05", "swap_ab": 1, "stream_k": 0, "pair": 0, "block_n": 0,
+                                 "balanced": 0}
+            continue
+        label = f"n{bn}{'-sk' if sk else ''}{'-pair' if pair else ''}"
+        yield label, {"algo": "tcgen05", "swap_ab": swap, "stream_k": sk, "pair": pair, "block_n": bn}
 
 
 def _time(call, iters, flush, stream):
@@ -136,7 +142,7 @@ def _plan_label(pl: dict) -> str:
     if pl["threads"] != 384:
         return "thin-input"
     if pl["swap_ab"]:
-        return "swap"
+        return "swap" if pl.get("balanced") else "swap-tiles"
     return f"n{pl['block_n']}{'-sk' if pl['stream_k'] else ''}{'-pair' if pl['cluster'] == 2 else ''}"
 
 

@@ -238,6 +238,8 @@ typedef struct cbs_plan_info {
     int swap_ab;      /* 1 when the GEMM runs transposed: channels on the MMA's M side, pixels on N */
     int cluster;      /* CTAs per cluster: 2 when CTA pairs run the 2-CTA MMA, each holding half of every weight tile */
     long long workspace_bytes; /* library-held scratch for stream-K partial tiles (0 if none) */
+    int balanced;     /* swap_ab only: 1 when each CTA takes an equal run of 32-pixel chunks (units of at
+                         most 256 pixels) instead of whole 256-pixel tiles */
 } cbs_plan_info;
 
 /* Fills `info` for the given shape, algorithm and SM count (sm_count > 0;
@@ -265,6 +267,8 @@ typedef struct cbs_plan_request {
                                   CBS_ERR_TIMEOUT, and later calls run normally.  (A bound of a
                                   few nanoseconds makes the waits run out on purpose: the watchdog
                                   test.)  Ignored by the other kernels. */
+    int balanced; /* -1, or (channel-major tiles only) 0: whole 256-pixel tiles dealt round-robin,
+                     1: each CTA an equal run of 32-pixel chunks */
 } cbs_plan_request;
 
 /* conv_bn_silu_plan with overrides.  CBS_ERR_INVALID_ARG for an out-of-range

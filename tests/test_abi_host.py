@@ -211,10 +211,30 @@ def test_plan_request_overrides(lib):
         lib.plan_request(1, 32, 32, 16, 32, 3, 3, 1, 1, stream_k=1)
     with pytest.raises(lib.CbsError):                                     # thin-input kernel: no tilings
         lib.plan_request(1, 640, 640, 3, 16, 3, 3, 2, 1, swap_ab=0)
-    for bad in ({"swap_ab": 2}, {"pair": -2}, {"block_n": 48}, {"wait_timeout_ns": -1}):
+    for bad in ({"swap_ab": 2}, {"pair": -2}, {"block_n": 48}, {"wait_timeout_ns": -1}, {"balanced": 2}):
         with pytest.raises(lib.CbsError) as e:
             lib.plan_request(*down, **bad)
         assert e.value.status == lib.CBS_ERR_INVALID_ARG
+
+
+def test_balanced_channel_major_plans(lib):
+    """Channel-major (swap AB) plans deal equal runs of 32-pixel chunks by default; whole
+    256-pixel tiles on request; a balanced run is refused on pixel-major tiles."""
+    pointwise = (16, 40, 40, 256, 256, 1, 1, 1, 0)   # 200 whole tiles: 48 CTAs would take two
+    p = lib.plan_request(*pointwise)
+    assert p["swap_ab"] == 1 and p["balanced"] == 1 and p["grid"] == 152
+    p0 = lib.plan_request(*pointwise, balanced=0)
+    assert p0["swap_ab"] == 1 and p0["balanced"] == 0 and p0["grid"] == 152 and p0["tiles"] == 200
+    assert lib.plan(*pointwise)["balanced"] == 1
+    tiny_swap = (2, 13, 11, 16, 24, 3, 3, 1, 1)      # 286 pixels: 9 chunks, so 9 CTAs
+    assert lib.plan_request(*tiny_swap, swap_ab=1)["grid"] == 9
+    assert lib.plan_request(*tiny_swap, swap_ab=1, balanced=0)["grid"] == 2
+    deep = (32, 20, 20, 512, 512, 3, 3, 1, 1)
+    assert lib.plan_request(*deep)["balanced"] == 0
+    assert lib.plan_request(*deep, balanced=0)["balanced"] == 0
+    with pytest.raises(lib.CbsError) as e:
+        lib.plan_request(*deep, balanced=1)
+    assert e.value.status == lib.CBS_ERR_UNSUPPORTED
 
 
 def test_tuning_sweep_variants_are_consistent():
@@ -225,5 +245,6 @@ def test_tuning_sweep_variants_are_consistent():
     for label, ov in vs[2:]:
         assert not (ov["pair"] and not ov["stream_k"])
         assert not (ov["swap_ab"] and (ov["stream_k"] or ov["pair"]))
+        assert ov.get("balanced", -1) != 1 or ov["swap_ab"] == 1
     assert len(tune.SWEEP) >= 15 and len({s.name for s in tune.SWEEP}) == len(tune.SWEEP)
 

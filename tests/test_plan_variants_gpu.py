@@ -32,6 +32,11 @@ CASES = [
     ("pw_n256", LayerShape("pw", 16, 40, 40, 256, 256, 1, 1, 1, 0), {"swap_ab": 0, "block_n": 256}),
     ("pw_n64", LayerShape("pw", 4, 40, 40, 256, 256, 1, 1, 1, 0), {"swap_ab": 0, "block_n": 64}),
     ("swap_small", LayerShape("ss", 2, 13, 11, 16, 24, 3, 3, 1, 1), {"swap_ab": 1}),
+    ("swap_small_tiles", LayerShape("ss", 2, 13, 11, 16, 24, 3, 3, 1, 1), {"swap_ab": 1, "balanced": 0}),
+    # balanced runs crossing from the first channel tile into a partial second one
+    ("swap_two_ctiles", LayerShape("bx", 3, 30, 30, 32, 200, 3, 3, 1, 1), {"swap_ab": 1}),
+    ("swap_multi_unit_tail", LayerShape("bl", 5, 37, 29, 64, 136, 3, 3, 1, 1), {"swap_ab": 1}),
+    ("pw_swap_tiles", LayerShape("pw", 4, 40, 40, 256, 256, 1, 1, 1, 0), {"swap_ab": 1, "balanced": 0}),
     ("direct", LayerShape("dd", 2, 13, 11, 16, 24, 3, 3, 1, 1), {"algo": "direct"}),
 ]
 
@@ -60,3 +65,22 @@ def test_forced_tiling_matches_oracle(capi, name, shape, overrides):
     bound = 1e-2 + 1e-2 * np.abs(ref)
     assert np.all(np.isfinite(got))
     assert np.all(err <= bound), (name, float((err - bound).max()))
+
+
+@pytest.mark.parametrize("shape", [LayerShape("pointwise", 16, 40, 40, 256, 256, 1, 1, 1, 0),
+                                   LayerShape("down", 16, 160, 160, 64, 128, 3, 3, 2, 1)],
+                         ids=["pointwise", "down"])
+def test_balanced_runs_equal_whole_tiles_bitwise(capi, shape):
+    """Balanced runs and whole tiles cut the pixels differently but sum every output's K
+    steps in the same order: the two schedules give bit-identical outputs."""
+    dev = torch.device("cuda:0")
+    inp = make_layer_inputs(shape, seed=67)
+    x = bits_to_torch_bf16(inp.x_bits).to(dev)
+    w = bits_to_torch_bf16(inp.w_bits).to(dev)
+    g, b, m, v = (torch.from_numpy(a).to(dev) for a in (inp.gamma, inp.beta, inp.mean, inp.var))
+    scale, bias = capi.fold(g, b, m, v, inp.eps)
+    y1 = capi.forward_request(x, w, scale, bias, shape.stride, shape.pad, swap_ab=1, balanced=1)
+    y0 = capi.forward_request(x, w, scale, bias, shape.stride, shape.pad, swap_ab=1, balanced=0)
+    torch.cuda.synchronize()
+    capi.check()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
