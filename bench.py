@@ -14,10 +14,12 @@ Timing: W warm-up steps, then K steps between two CUDA events on the
 launching stream, bracketed by a barrier and torch.cuda.synchronize() on
 both sides; max over ranks.  Inputs rotate over 3 buffer sets (about 426 MB
 touched per rotation, more than three times the 129 MB L2), so each step
-reads its data from HBM.  The step is replayed from CUDA graphs captured
+reads its data from HBM.  The step is replayed from one CUDA graph captured
 from the API calls (six launches through Python per step would make the host
-the bottleneck); the dominant layer's forward is its own graph, so CUDA events
-on the stream bracket exactly that kernel inside the timed region.  Per-layer
+the bottleneck).  The dominant layer's launch duration (the ``roofline``
+object) comes from a second timed run of the same steps whose graphs carry
+event-record nodes around that forward: the nodes cut the programmatic-launch
+overlap into it, so they stay out of the run that gives ``value``.  Per-layer
 times in ``per_layer`` come from two separate passes: each call alone with the
 L2 flushed before it, and each layer's forward back to back in a CUDA graph
 over enough buffer sets that their rotation exceeds the L2.  SM clocks and throttle reasons are sampled with nvidia-smi during
@@ -295,43 +297,36 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     capi.check(stream)
 
-    # One CUDA graph per segment per buffer set.
-    plan = []
-    for i in range(ROTATION):
-        pre, dom, post = segments(i)
-        parts = []
-        for calls in (pre, [dom], post):
-            if not calls:
-                parts.append(None)
-            elif args.no_graphs:
-                parts.append(calls)
-            else:
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    for f in calls:
-                        f(None)
-                parts.append(g)
-        plan.append(parts)
+    # The timed steps: one CUDA graph per buffer set holding the whole step (or, with
+    # --no-graphs, the API calls themselves, with events recorded around the dominant
+    # layer's forward).
+    def capture(calls):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for f in calls:
+                f(None)
+        return g
+
+    if args.no_graphs:
+        plan = [segments(i) for i in range(ROTATION)]
+    else:
+        plan = [capture(pre + [dom] + post) for pre, dom, post in (segments(i) for i in range(ROTATION))]
     torch.cuda.synchronize()
 
-    def run_part(part):
-        if part is None:
-            return
-        if isinstance(part, list):
-            for f in part:
-                f(stream)
-        else:
-            part.replay()
-
     def step(i, ev=None):
+        if not args.no_graphs:
+            plan[i % ROTATION].replay()
+            return
         pre, dom, post = plan[i % ROTATION]
-        run_part(pre)
+        for f in pre:
+            f(stream)
         if ev is not None:
             ev[0].record(stream)
-        run_part(dom)
+        dom(stream)
         if ev is not None:
             ev[1].record(stream)
-        run_part(post)
+        for f in post:
+            f(stream)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -341,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
 
     K = args.steps
     dom_ev = ([torch.cuda.Event(enable_timing=True) for _ in range(K)],
-              [torch.cuda.Event(enable_timing=True) for _ in range(K)])
+              [torch.cuda.Event(enable_timing=True) for _ in range(K)]) if args.no_graphs else None
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(device_uuid(local_rank))
@@ -352,7 +347,7 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         start.record(stream)
         for i in range(K):
-            step(i, (dom_ev[0][i], dom_ev[1][i]))
+            step(i, None if dom_ev is None else (dom_ev[0][i], dom_ev[1][i]))
         end.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -361,7 +356,12 @@ def run_ours(args, rank, world, local_rank):
     capi.check(stream)
     elapsed_s = start.elapsed_time(end) / 1e3
     elapsed_max = max_over_ranks(elapsed_s, world, dev)
-    dom_us = 1e3 * float(np.mean([a.elapsed_time(b) for a, b in zip(*dom_ev)]))
+    if dom_ev is not None:
+        dom_us, dom_how = 1e3 * float(np.mean([a.elapsed_time(b) for a, b in zip(*dom_ev)])), \
+            f"events around the forward in each of the {K} timed steps"
+    else:
+        dom_us, dom_how = dominant_in_step(segments, capture, stream, args.warmup, min(K, 600))
+    capi.check(stream)
 
     peaks, peak_src = load_peaks()
     b2b = layer_times_back_to_back(capi, sets, inputs, layers, stream, dev,
@@ -400,6 +400,7 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(dominant),
                 "kernel": f"{dominant} layer forward ({per_layer[dominant]['kernel']})",
                 "launch_us": round(dom_us, 3),
+                "launch_timing": dom_how,
                 "peak_source": f"{peak_src} ({'bf16 dense burst' if bound == 'tensor' else 'HBM copy'})",
                 **per_launch}
 
@@ -429,7 +430,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": f"{ROTATION} rotating buffer sets (~426 MB per rotation > 129 MB L2); "
                          "per_layer times: L2 flushed (512 MB write) before each call",
                    "launch": ("direct API calls" if args.no_graphs else
-                              "CUDA graphs captured from the API calls, replayed per step"),
+                              "one CUDA graph per step captured from the API calls, replayed"),
                    "parallelism": f"replicas x{world} (each rank runs the full step)"},
         "roofline": roofline,
         "per_layer": per_layer,
@@ -453,6 +454,93 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(world)
+
+
+def _cu_event_record_external():
+    """cuEventRecordWithFlags from the CUDA driver, or None."""
+    import ctypes
+    try:
+        lib = ctypes.CDLL("libcuda.so.1")
+        fn = lib.cuEventRecordWithFlags
+    except (OSError, AttributeError):
+        return None
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+def dominant_in_step(segments, capture, stream, warmup, steps):
+    """Launch duration of the dominant layer's forward inside the step: a second timed
+    run of `steps` steps whose graphs carry event-record nodes around that forward.  The
+    nodes cut the programmatic-launch edge into the forward, so they stay out of the run
+    that gives the step's throughput.  Where the driver refuses the nodes, the step is
+    split into three graphs with events recorded between their launches."""
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(ROTATION)]
+    graphs = capture_steps_with_events(segments, events, stream)
+    with torch.cuda.stream(stream):
+        if graphs is not None:
+            for i in range(warmup + steps):
+                graphs[i % ROTATION].replay()
+            torch.cuda.synchronize()
+            us = 1e3 * float(np.mean([a.elapsed_time(b) for a, b in events]))
+            return us, (f"event-record nodes around the forward inside the step's graph; {steps} timed "
+                        f"steps, the last replay of each of the {ROTATION} buffer sets' graphs")
+        split = []
+        for i in range(ROTATION):
+            pre, dom, post = segments(i)
+            split.append((capture(pre) if pre else None, capture([dom]), capture(post) if post else None))
+        evs = []
+        for i in range(warmup + steps):
+            pre, dom, post = split[i % ROTATION]
+            if pre is not None:
+                pre.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dom.replay()
+            b.record(stream)
+            if post is not None:
+                post.replay()
+            if i >= warmup:
+                evs.append((a, b))
+        torch.cuda.synchronize()
+    us = 1e3 * float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    return us, f"events between graph launches around the forward; {steps} timed steps"
+
+
+def capture_steps_with_events(segments, events, stream):
+    """One CUDA graph per buffer set holding the whole step, with an event-record node
+    (CU_EVENT_RECORD_EXTERNAL) on each side of the dominant layer's forward, so that
+    CUDA events on the launching stream bracket that kernel in every replay without
+    splitting the step into several graphs.  None if the driver refuses the nodes."""
+    record = _cu_event_record_external()
+    if record is None:
+        return None
+    for a, b in events:          # torch creates the CUDA events on first use
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    graphs = []
+    try:
+        for i, (a, b) in enumerate(events):
+            pre, dom, post = segments(i)
+            g = torch.cuda.CUDAGraph()
+            rc = 0
+            with torch.cuda.graph(g, stream=stream):
+                for f in pre:
+                    f(None)
+                rc |= record(a.cuda_event, stream.cuda_stream, 1)
+                dom(None)
+                rc |= record(b.cuda_event, stream.cuda_stream, 1)
+                for f in post:
+                    f(None)
+            if rc != 0:
+                return None
+            graphs.append(g)
+    except RuntimeError:
+        torch.cuda.synchronize()
+        return None
+    return graphs
 
 
 def layer_times_back_to_back(capi, sets, inputs, layers, stream, dev, replays) -> dict:
