@@ -29,6 +29,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "cbs_internal.h"
 #include "epilogue.cuh"
@@ -215,7 +216,7 @@ struct TcCfg {
     static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN;
     static constexpr int ROW_A = BK * 2;  // operand row bytes = swizzle span
     static constexpr int SMEM_LIMIT = 232448;
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 512;
     static constexpr int STAGES_FIT =
         (SMEM_LIMIT - 1024 - STG_TOTAL - BAR_BYTES) / (A_STRIDE + B_STRIDE);
     static constexpr int STAGES = STAGES_FIT < 8 ? STAGES_FIT : 8;
@@ -272,11 +273,29 @@ __device__ __forceinline__ void prefetch_l2(const void *p)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Calls f(std::integral_constant<int, mode>) with the epilogue mode as a compile-time
+// constant: SiLU alone for the fused layer's instantiation, else one arm per mode.
+template <int EPI, typename F>
+__device__ __forceinline__ void with_epi_mode(int mode, F &&f)
+{
+    if constexpr (EPI == kEpiKindSilu) {
+        f(std::integral_constant<int, kEpiSilu>{});
+    } else {
+        switch (mode) {
+        case kEpiConvOnly: f(std::integral_constant<int, kEpiConvOnly>{}); break;
+        case kEpiBn: f(std::integral_constant<int, kEpiBn>{}); break;
+        case kEpiRelu: f(std::integral_constant<int, kEpiRelu>{}); break;
+        default: f(std::integral_constant<int, kEpiSilu>{}); break;
+        }
+    }
+}
+
 template <int BN, int BK, bool SWAP, bool PAIR, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_conv_bn_silu_kernel(const __grid_constant__ CUtensorMap tm_x,
                            const __grid_constant__ CUtensorMap tm_w,
-                           const __grid_constant__ CUtensorMap tm_y, const TcArgs a)
+                           const __grid_constant__ CUtensorMap tm_y,
+                           const __grid_constant__ CUtensorMap tm_r, const TcArgs a)
 {
     static_assert(!(SWAP && PAIR), "CTA pairs serve the pixel-major (unswapped) tile only");
     static_assert(!SWAP || TcCfg<BN, BK>::EC == 32, "channel-major units are cut in 32-pixel chunks");
@@ -300,7 +319,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *rbar = drain + 1;  // residual epilogue: a load barrier per staging buffer of each epilogue warp
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rbar + 2 * C::EPI_WARPS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -320,6 +340,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             dev::mbar_init(dev::smem_u32(&tempty[i]), PAIR ? 2 * C::EPI_WARPS : C::EPI_WARPS);
         }
         dev::mbar_init(dev::smem_u32(drain), 1);
+        if constexpr (RES)
+            for (int i = 0; i < 2 * C::EPI_WARPS; ++i) dev::mbar_init(dev::smem_u32(&rbar[i]), 1);
         *abort_flag = 0;
         dev::fence_mbarrier_init();
     }
@@ -327,6 +349,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         dev::prefetch_tensormap(&tm_x);
         dev::prefetch_tensormap(&tm_w);
         dev::prefetch_tensormap(&tm_y);
+        if constexpr (RES) dev::prefetch_tensormap(&tm_r);
     }
     if (warp == 1) {
         // CG = 2: collective over the pair (warp 1 of both CTAs); same columns in both.
@@ -525,6 +548,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint8_t *my_stg = sm_stg + ep * 2 * C::STG_BYTES;
         int sbuf = 0;
         int lt = 0;
+        // Residual epilogue: the residual's tile for a chunk is loaded by TMA into the
+        // staging buffer the chunk's output will be stored from (the same box of the
+        // same-shaped tensor), while the chunk's accumulator is read and activated.
+        uint32_t r_phase = 0;    // per staging buffer: parity of its load barrier's next phase
+        uint32_t r_pending = 0;  // per staging buffer: a load issued and not yet waited for
+        auto residual_load = [&](int c0, int c1) {
+            if (lane == 0) {
+                dev::bulk_wait_group_read<1>();  // the buffer's previous store has read it
+                const uint32_t bar = dev::smem_u32(&rbar[2 * ep + sbuf]);
+                dev::mbar_arrive_expect_tx(bar, C::STG_BYTES);
+                dev::tma_load_2d(dev::smem_u32(my_stg + sbuf * C::STG_BYTES), &tm_r, bar, c0, c1);
+            }
+            r_pending |= 1u << sbuf;
+            __syncwarp();
+        };
+        auto residual_wait = [&]() {
+            const uint32_t bar = dev::smem_u32(&rbar[2 * ep + sbuf]);
+            const bool ok = dev::mbar_wait_bounded(bar, (r_phase >> sbuf) & 1u, abort_flag, a.wait_ns);
+            r_phase ^= 1u << sbuf;
+            r_pending &= ~(1u << sbuf);
+            if (!__all_sync(0xffffffffu, ok) && lane == 0 && !*abort_flag)
+                record_error(kErrTimeoutEpilogue, abort_flag);
+        };
         const int row = ew * 32 + lane;  // this thread's row of the tile (TMEM lane)
         WorkIter wi(a, vb, vg);
         WorkUnit u;
@@ -615,6 +661,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
 #pragma unroll 1
                 for (int j = half; j < nchunks; j += C::SPLIT) {
+                    if constexpr (RES) residual_load(ch_w0, p0 + j * EC);
                     uint32_t v[EC];
 #pragma unroll
                     for (int q = 0; q < EC / 16; ++q)
@@ -632,25 +679,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     __syncwarp();
                     __nv_bfloat16 *sb = reinterpret_cast<__nv_bfloat16 *>(my_stg + sbuf * C::STG_BYTES);
                     const int px0 = p0 + j * EC;
-                    if constexpr (RES) {
-                        // Residual of this lane's channel for the chunk's pixels (across the
-                        // warp, one 64-byte run of channels per pixel), all loaded first.
-                        float rv[EC];
+                    with_epi_mode<EPI>(emode, [&](auto mode_c) {
+                        constexpr int md = decltype(mode_c)::value;
+                        if constexpr (RES) {
+                            // The residual tile is in the staging buffer (row pp: the pixel's 32
+                            // channels); each lane adds its channel's column in place.
+                            float f[EC];
 #pragma unroll
-                        for (int pp = 0; pp < EC; ++pp)
-                            rv[pp] = (ch < a.c_out && px0 + pp < a.m)
-                                         ? __bfloat162float(__ldg(a.residual + (size_t)(px0 + pp) * a.c_out + ch))
-                                         : 0.f;
+                            for (int pp = 0; pp < EC; ++pp)
+                                f[pp] = dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, md);
+                            residual_wait();
 #pragma unroll
-                        for (int pp = 0; pp < EC; ++pp)
-                            sb[pp * 32 + lane] = __float2bfloat16_rn(
-                                dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, emode) + rv[pp]);
-                    } else {
+                            for (int pp = 0; pp < EC; ++pp)
+                                sb[pp * 32 + lane] =
+                                    __float2bfloat16_rn(f[pp] + __bfloat162float(sb[pp * 32 + lane]));
+                        } else {
 #pragma unroll
-                        for (int pp = 0; pp < EC; ++pp)  // row pp: 32 channels, one per lane
-                            sb[pp * 32 + lane] = __float2bfloat16_rn(
-                                dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, emode));
-                    }
+                            for (int pp = 0; pp < EC; ++pp)  // row pp: 32 channels, one per lane
+                                sb[pp * 32 + lane] = __float2bfloat16_rn(
+                                    dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, md));
+                        }
+                    });
                     dev::fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0 && px0 < a.m && ch_w0 < a.c_out) {
@@ -699,6 +748,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN + col_base);
 #pragma unroll 1
             for (int j = 0; j < C::EPI_COLS / EC; ++j) {
+                if constexpr (RES)
+                    if (!publish) residual_load(n0 + col_base + j * EC, row0);
                 uint32_t v[EC];
 #pragma unroll
                 for (int q = 0; q < EC / 16; ++q)
@@ -739,72 +790,86 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int ch0 = n0 + col_base + j * EC;
                 uint32_t packed[EC / 2];
                 uint32_t q8[FP8 ? EC / 4 : 1];
-                if constexpr (FP8) {
-                    // fp8 output: each value rounded once, from fp32 straight to e4m3.
+                // The activation is a compile-time constant in each arm: the fused layer's
+                // instantiation has SiLU alone; the others pick the arm once per chunk.
+                auto activate = [&](auto mode_c) {
+                    constexpr int md = decltype(mode_c)::value;
+                    if constexpr (FP8) {
+                        // fp8 output: each value rounded once, from fp32 straight to e4m3.
 #pragma unroll
-                    for (int i = 0; i < EC; i += 4) {
-                        float f[4];
+                        for (int i = 0; i < EC; i += 4) {
+                            float f[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = ch0 + i + e;
-                            f[e] = c < a.c_out ? dev::epilogue_value(__uint_as_float(v[i + e]), __ldg(a.scale + c),
-                                                                     __ldg(a.bias + c), emode)
-                                               : 0.f;
+                            for (int e = 0; e < 4; ++e) {
+                                const int c = ch0 + i + e;
+                                f[e] = c < a.c_out ? dev::epilogue_value(__uint_as_float(v[i + e]), __ldg(a.scale + c),
+                                                                         __ldg(a.bias + c), md)
+                                                   : 0.f;
+                            }
+                            q8[i / 4] = dev::pack_e4m3x4(f[0], f[1], f[2], f[3]);
                         }
-                        q8[i / 4] = dev::pack_e4m3x4(f[0], f[1], f[2], f[3]);
-                    }
-                } else if constexpr (RES) {
-                    // With a residual: this lane's pixel row, channels ch0.. (8 per 16-byte
-                    // load; c_out % 8 == 0, so a group of 8 is wholly inside or outside).
-                    const int pix = row0 + lane;
-                    uint4 rr[EC / 8];
+                    } else if constexpr (RES) {
+                        // With a residual: its tile is in the staging buffer, swizzled like the
+                        // output tile; this lane's row, 8 channels per 16-byte piece.
+                        float f[EC];
+                        if (ch0 + EC <= a.c_out) {
 #pragma unroll
-                    for (int g = 0; g < EC / 8; ++g)
-                        rr[g] = (pix < a.m && ch0 + 8 * g < a.c_out)
-                                    ? __ldg(reinterpret_cast<const uint4 *>(a.residual + (size_t)pix * a.c_out + ch0 +
-                                                                            8 * g))
-                                    : make_uint4(0u, 0u, 0u, 0u);
+                            for (int i = 0; i < EC; i += 4) {
+                                const float4 sc = __ldg(reinterpret_cast<const float4 *>(a.scale + ch0 + i));
+                                const float4 bi = __ldg(reinterpret_cast<const float4 *>(a.bias + ch0 + i));
+                                f[i] = dev::epilogue_value(__uint_as_float(v[i]), sc.x, bi.x, md);
+                                f[i + 1] = dev::epilogue_value(__uint_as_float(v[i + 1]), sc.y, bi.y, md);
+                                f[i + 2] = dev::epilogue_value(__uint_as_float(v[i + 2]), sc.z, bi.z, md);
+                                f[i + 3] = dev::epilogue_value(__uint_as_float(v[i + 3]), sc.w, bi.w, md);
+                            }
+                        } else {
 #pragma unroll
-                    for (int i = 0; i < EC; i += 8) {
-                        const uint32_t rw[4] = {rr[i / 8].x, rr[i / 8].y, rr[i / 8].z, rr[i / 8].w};
+                            for (int i = 0; i < EC; ++i) {
+                                const int c = ch0 + i;
+                                f[i] = c < a.c_out ? dev::epilogue_value(__uint_as_float(v[i]), __ldg(a.scale + c),
+                                                                         __ldg(a.bias + c), md)
+                                                   : 0.f;
+                            }
+                        }
+                        residual_wait();
+                        const uint8_t *rb = my_stg + sbuf * C::STG_BYTES;
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            const int c = ch0 + i + e;
-                            const float f0 = c < a.c_out ? dev::epilogue_value(__uint_as_float(v[i + e]), __ldg(a.scale + c),
-                                                                               __ldg(a.bias + c), emode)
-                                                         : 0.f;
-                            const float f1 = c + 1 < a.c_out
-                                                 ? dev::epilogue_value(__uint_as_float(v[i + e + 1]), __ldg(a.scale + c + 1),
-                                                                       __ldg(a.bias + c + 1), emode)
-                                                 : 0.f;
-                            packed[(i + e) / 2] = dev::pack_bf16x2(f0 + __uint_as_float(rw[e / 2] << 16),
-                                                                   f1 + __uint_as_float(rw[e / 2] & 0xffff0000u));
+                        for (int q = 0; q < ROW_Y / 16; ++q) {
+                            const uint4 r4 = *reinterpret_cast<const uint4 *>(
+                                rb + swizzle_offset<ROW_Y>((uint32_t)(lane * ROW_Y + q * 16)));
+                            const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                packed[4 * q + e] = dev::pack_bf16x2(f[8 * q + 2 * e] + __uint_as_float(rw[e] << 16),
+                                                                     f[8 * q + 2 * e + 1] +
+                                                                         __uint_as_float(rw[e] & 0xffff0000u));
+                        }
+                    } else if (ch0 + EC <= a.c_out) {
+#pragma unroll
+                        for (int i = 0; i < EC; i += 4) {
+                            const float4 sc = __ldg(reinterpret_cast<const float4 *>(a.scale + ch0 + i));
+                            const float4 bi = __ldg(reinterpret_cast<const float4 *>(a.bias + ch0 + i));
+                            packed[i / 2] = dev::pack_bf16x2(
+                                dev::epilogue_value(__uint_as_float(v[i]), sc.x, bi.x, md),
+                                dev::epilogue_value(__uint_as_float(v[i + 1]), sc.y, bi.y, md));
+                            packed[i / 2 + 1] =
+                                dev::pack_bf16x2(dev::epilogue_value(__uint_as_float(v[i + 2]), sc.z, bi.z, md),
+                                                 dev::epilogue_value(__uint_as_float(v[i + 3]), sc.w, bi.w, md));
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < EC; i += 2) {
+                            const int c0 = ch0 + i, c1 = ch0 + i + 1;
+                            const float s0 = c0 < a.c_out ? __ldg(a.scale + c0) : 0.f;
+                            const float b0 = c0 < a.c_out ? __ldg(a.bias + c0) : 0.f;
+                            const float s1 = c1 < a.c_out ? __ldg(a.scale + c1) : 0.f;
+                            const float b1 = c1 < a.c_out ? __ldg(a.bias + c1) : 0.f;
+                            packed[i / 2] = dev::pack_bf16x2(dev::epilogue_value(__uint_as_float(v[i]), s0, b0, md),
+                                                             dev::epilogue_value(__uint_as_float(v[i + 1]), s1, b1, md));
                         }
                     }
-                } else if (ch0 + EC <= a.c_out) {
-#pragma unroll
-                    for (int i = 0; i < EC; i += 4) {
-                        const float4 sc = __ldg(reinterpret_cast<const float4 *>(a.scale + ch0 + i));
-                        const float4 bi = __ldg(reinterpret_cast<const float4 *>(a.bias + ch0 + i));
-                        packed[i / 2] = dev::pack_bf16x2(
-                            dev::epilogue_value(__uint_as_float(v[i]), sc.x, bi.x, emode),
-                            dev::epilogue_value(__uint_as_float(v[i + 1]), sc.y, bi.y, emode));
-                        packed[i / 2 + 1] =
-                            dev::pack_bf16x2(dev::epilogue_value(__uint_as_float(v[i + 2]), sc.z, bi.z, emode),
-                                             dev::epilogue_value(__uint_as_float(v[i + 3]), sc.w, bi.w, emode));
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < EC; i += 2) {
-                        const int c0 = ch0 + i, c1 = ch0 + i + 1;
-                        const float s0 = c0 < a.c_out ? __ldg(a.scale + c0) : 0.f;
-                        const float b0 = c0 < a.c_out ? __ldg(a.bias + c0) : 0.f;
-                        const float s1 = c1 < a.c_out ? __ldg(a.scale + c1) : 0.f;
-                        const float b1 = c1 < a.c_out ? __ldg(a.bias + c1) : 0.f;
-                        packed[i / 2] = dev::pack_bf16x2(dev::epilogue_value(__uint_as_float(v[i]), s0, b0, emode),
-                                                         dev::epilogue_value(__uint_as_float(v[i + 1]), s1, b1, emode));
-                    }
-                }
+                };
+                with_epi_mode<EPI>(emode, activate);
                 // Stage the warp's 32 rows x EC channels, then one TMA store.
                 if (lane == 0) dev::bulk_wait_group_read<1>();
                 __syncwarp();
@@ -846,6 +911,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     a.flags[slot * kTcFlagsPerSlot + kTcTicketOffset + ep] = 0;
                 }
             }
+        }
+        if constexpr (RES) {
+            // Only after a wait ran out can a load still be in flight: wait for it once more
+            // (bounded) before the CTA's shared memory is given up.
+            for (int b = 0; b < 2; ++b)
+                if ((r_pending >> b) & 1u) {
+                    const bool ok = dev::mbar_wait_bounded(dev::smem_u32(&rbar[2 * ep + b]), (r_phase >> b) & 1u,
+                                                           nullptr, kWaitTimeoutNs);
+                    if (!ok && lane == 0) record_error(kErrTimeoutDrain, abort_flag);
+                }
         }
         if (lane == 0) dev::bulk_wait_group<0>();
         __syncwarp();
@@ -895,7 +970,28 @@ CUtensorMapSwizzle swizzle_for_row_bytes(int row_bytes)
 
 struct TcMaps {
     CUtensorMap x, w, y;
+    CUtensorMap r;  // the residual, laid out and boxed like y (a copy of y's map when there is none)
 };
+
+// A bf16 NHWC tensor shaped like y ([m][c_out]) at `base`, viewed as (C_out, M) with the
+// epilogue's store box: (EC, 32) with the EC-channel swizzle, or for swap AB (32, EC),
+// unswizzled 64-byte rows.  y itself, and the residual the epilogue adds, which it
+// loads tile by tile into the same staging buffer that y's tile is stored from.
+static cudaError_t encode_bf16_like_y(const ConvProblem &p, int block_n, bool swap, const void *base,
+                                      CUtensorMap *out)
+{
+    int split = 1, ec = 16;
+    tc_epilogue_geometry(block_n, &split, &ec);
+    cuuint64_t dims[2] = {(cuuint64_t)p.c_out, (cuuint64_t)p.m};
+    cuuint64_t strides[1] = {(cuuint64_t)p.c_out * 2};
+    cuuint32_t box[2] = {(cuuint32_t)(swap ? 32 : ec), (cuuint32_t)(swap ? ec : 32)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode_tiled(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                swap ? CU_TENSOR_MAP_SWIZZLE_NONE : swizzle_for_row_bytes(ec * 2),
+                                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swap, bool pair, TcMaps *maps)
 {
@@ -949,23 +1045,12 @@ cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swa
                                     ec == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        maps->r = maps->y;
         return cudaSuccess;
     }
-    {
-        int split = 1, ec = 16;
-        tc_epilogue_geometry(block_n, &split, &ec);
-        cuuint64_t dims[2] = {(cuuint64_t)p.c_out, (cuuint64_t)p.m};
-        cuuint64_t strides[1] = {(cuuint64_t)p.c_out * 2};
-        // Swap AB: 32 channels x `ec` pixels, unswizzled 64-byte rows.
-        cuuint32_t box[2] = {(cuuint32_t)(swap ? 32 : ec), (cuuint32_t)(swap ? ec : 32)};
-        cuuint32_t estr[2] = {1, 1};
-        CUresult r = g_encode_tiled(&maps->y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.y, dims, strides,
-                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                    swap ? CU_TENSOR_MAP_SWIZZLE_NONE : swizzle_for_row_bytes(ec * 2),
-                                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
-    return cudaSuccess;
+    st = encode_bf16_like_y(p, block_n, swap, p.y, &maps->y);
+    maps->r = maps->y;
+    return st;
 }
 
 // Encoded tensor maps of recent calls, keyed by pointers, shape and tile.  Encoding
@@ -1138,7 +1223,7 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
         a.partial = reinterpret_cast<float *>(static_cast<char *>(ws) + plan.flag_bytes);
     }
     return launch_overlapped(kern, dim3((unsigned)plan.grid), dim3(kTcThreads), (size_t)C::SMEM, stream,
-                             PAIR ? 2 : 1, maps.x, maps.w, maps.y, a);
+                             PAIR ? 2 : 1, maps.x, maps.w, maps.y, maps.r, a);
 }
 
 }  // namespace
@@ -1154,14 +1239,14 @@ int tc_smem_bytes(int block_n, int block_k, int stages, int pair)
 {
     const int a = (kTcBlockM * block_k * 2 + 1023) / 1024 * 1024;
     const int b = ((pair ? block_n / 2 : block_n) * block_k * 2 + 1023) / 1024 * 1024;
-    return 1024 + stages * (a + b) + staging_bytes(block_n) + 256;
+    return 1024 + stages * (a + b) + staging_bytes(block_n) + 512;
 }
 
 static int stages_for(int block_n, int block_k, int pair = 0)
 {
     const int a = (kTcBlockM * block_k * 2 + 1023) / 1024 * 1024;
     const int b = ((pair ? block_n / 2 : block_n) * block_k * 2 + 1023) / 1024 * 1024;
-    const int fit = (232448 - 1024 - staging_bytes(block_n) - 256) / (a + b);
+    const int fit = (232448 - 1024 - staging_bytes(block_n) - 512) / (a + b);
     return fit < 8 ? fit : 8;
 }
 
@@ -1408,7 +1493,13 @@ cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, c
         if (p.residual != nullptr || plan.swap_ab) return cudaErrorInvalidConfiguration;
         return dispatch<kEpiKindFp8>(p, plan, maps, stream, workspace);
     }
-    if (p.residual != nullptr) return dispatch<kEpiKindResidual>(p, plan, maps, stream, workspace);
+    if (p.residual != nullptr) {
+        // The residual's map changes with its pointer: encoded per call (a host call
+        // of a few microseconds, next to the cached maps).
+        st = encode_bf16_like_y(p, plan.block_n, plan.swap_ab != 0, p.residual, &maps.r);
+        if (st != cudaSuccess) return st;
+        return dispatch<kEpiKindResidual>(p, plan, maps, stream, workspace);
+    }
     if (p.epi_mode != kEpiSilu) return dispatch<kEpiKindMode>(p, plan, maps, stream, workspace);
     return dispatch<kEpiKindSilu>(p, plan, maps, stream, workspace);
 }

@@ -34,6 +34,7 @@ SHAPES = [
     (LayerShape("ragged", 2, 13, 11, 16, 24, 3, 3, 1, 1), "tcgen05 pixel-major, channel tail"),
     (LayerShape("swap", 2, 100, 100, 16, 80, 3, 3, 1, 1), "tcgen05 channel-major (swap AB)"),
     (LayerShape("pairs", 31, 20, 20, 128, 512, 3, 3, 1, 1), "tcgen05 2-CTA stream-K"),
+    (LayerShape("c2f", 8, 80, 80, 128, 128, 1, 1, 1, 0), "tcgen05 channel-major, balanced runs"),
     (LayerShape("thin", 1, 64, 64, 3, 16, 3, 3, 2, 1), "thin-input tcgen05"),
     (LayerShape("direct", 1, 9, 7, 5, 12, 3, 3, 2, 1), "CUDA-core direct"),
 ]
@@ -87,7 +88,7 @@ def test_epilogue_matches_oracle(capi, shape, what, activation, with_residual):
     _check(got, ref, f"{shape.name} ({what}) {activation} residual={with_residual}")
 
 
-@pytest.mark.parametrize("name", ["tiny", "swap", "thin", "direct"])
+@pytest.mark.parametrize("name", ["tiny", "swap", "pairs", "c2f", "thin", "direct"])
 def test_residual_in_place(capi, name):
     """residual == y: each element's residual is read before its result is stored."""
     shape = next(s for s, _ in SHAPES if s.name == name)
