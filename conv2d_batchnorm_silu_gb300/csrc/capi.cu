@@ -120,7 +120,7 @@ int launch_forward(const cbs::ConvProblem &p, int algo, cudaStream_t strm, const
         cudaError_t e = cbs::tc_launch(p, plan, strm);
         return e == cudaSuccess ? CBS_OK : cuda_fail(e);
     }
-    if (has_overrides(rq) && !p.out_fp8) return CBS_ERR_UNSUPPORTED;
+    if (has_overrides(rq)) return CBS_ERR_UNSUPPORTED;
     cudaError_t e = cbs::direct_launch(p, strm);
     return e == cudaSuccess ? CBS_OK : cuda_fail(e);
 }
@@ -329,9 +329,7 @@ int conv_bn_act_forward_fp8(const void *x, const void *w, const float *scale, co
     p.y = y;
     p.epi_mode = mode;
     p.out_fp8 = 1;
-    // Pixel-major tiles only: the channel-major (swap AB) epilogue writes bf16.
-    const cbs::PlanRequest rq{0, -1, -1, 0, -1};
-    return launch_forward(p, CBS_ALGO_AUTO, static_cast<cudaStream_t>(stream), &rq);
+    return launch_forward(p, CBS_ALGO_AUTO, static_cast<cudaStream_t>(stream));
 }
 
 int conv_bn_silu_forward_unfused(const void *x, const void *w, const float *scale, const float *bias,

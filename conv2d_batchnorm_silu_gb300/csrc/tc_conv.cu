@@ -301,7 +301,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     static_assert(!SWAP || TcCfg<BN, BK>::EC == 32, "channel-major units are cut in 32-pixel chunks");
     constexpr bool RES = EPI == kEpiKindResidual;
     constexpr bool FP8 = EPI == kEpiKindFp8;
-    static_assert(!(FP8 && SWAP), "the fp8 output is written by the pixel-major epilogue");
     // The epilogue mode: a compile-time constant for the fused layer.
     const int emode = EPI == kEpiKindSilu ? (int)kEpiSilu : a.epi_mode;
     constexpr int CG = PAIR ? 2 : 1;  // tcgen05 CTA group
@@ -678,10 +677,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) dev::bulk_wait_group_read<1>();
                     __syncwarp();
                     __nv_bfloat16 *sb = reinterpret_cast<__nv_bfloat16 *>(my_stg + sbuf * C::STG_BYTES);
+                    uint8_t *sb8 = my_stg + sbuf * C::STG_BYTES;  // fp8: rows of 32 one-byte channels
                     const int px0 = p0 + j * EC;
                     with_epi_mode<EPI>(emode, [&](auto mode_c) {
                         constexpr int md = decltype(mode_c)::value;
-                        if constexpr (RES) {
+                        if constexpr (FP8) {
+#pragma unroll
+                            for (int pp = 0; pp < EC; ++pp)  // row pp: 32 channels, one byte per lane
+                                sb8[pp * 32 + lane] =
+                                    dev::to_e4m3(dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, md));
+                        } else if constexpr (RES) {
                             // The residual tile is in the staging buffer (row pp: the pixel's 32
                             // channels); each lane adds its channel's column in place.
                             float f[EC];
@@ -1033,16 +1038,17 @@ cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swa
     }
     // y: (C_out, M), box (EC, 32): one epilogue warp's rows, one column chunk.
     if (p.out_fp8) {
-        // fp8 e4m3 output, one byte per element: rows of EC bytes.
+        // fp8 e4m3 output, one byte per element: rows of EC bytes (pixel-major), or for
+        // swap AB rows of 32 one-byte channels, EC pixels (unswizzled).
         int split = 1, ec = 16;
         tc_epilogue_geometry(block_n, &split, &ec);
         cuuint64_t dims[2] = {(cuuint64_t)p.c_out, (cuuint64_t)p.m};
         cuuint64_t strides[1] = {(cuuint64_t)p.c_out};
-        cuuint32_t box[2] = {(cuuint32_t)ec, 32};
+        cuuint32_t box[2] = {(cuuint32_t)(swap ? 32 : ec), (cuuint32_t)(swap ? ec : 32)};
         cuuint32_t estr[2] = {1, 1};
         CUresult r = g_encode_tiled(&maps->y, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.y, dims, strides, box, estr,
                                     CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                    ec == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    (!swap && ec == 32) ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
         maps->r = maps->y;
@@ -1452,15 +1458,11 @@ cudaError_t dispatch(const ConvProblem &p, const TcPlan &plan, const TcMaps &map
                      void *workspace)
 {
     if (plan.swap_ab) {
-        if constexpr (EPI == kEpiKindFp8) {
-            return cudaErrorInvalidConfiguration;  // the fp8 output is pixel-major only
-        } else {
         if (plan.block_n != 256) return cudaErrorInvalidConfiguration;
         if (plan.block_k == 64) return launch_cfg<256, 64, true, false, EPI>(p, plan, maps, stream, workspace);
         if (plan.block_k == 32) return launch_cfg<256, 32, true, false, EPI>(p, plan, maps, stream, workspace);
         if (plan.block_k == 16) return launch_cfg<256, 16, true, false, EPI>(p, plan, maps, stream, workspace);
         return cudaErrorInvalidConfiguration;
-        }
     }
     if (plan.pair) {
         if (plan.block_n != 256) return cudaErrorInvalidConfiguration;
@@ -1490,7 +1492,7 @@ cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, c
     cudaError_t st = cached_maps(p, plan.block_n, plan.block_k, plan.swap_ab != 0, plan.pair != 0, &maps);
     if (st != cudaSuccess) return st;
     if (p.out_fp8) {
-        if (p.residual != nullptr || plan.swap_ab) return cudaErrorInvalidConfiguration;
+        if (p.residual != nullptr) return cudaErrorInvalidConfiguration;
         return dispatch<kEpiKindFp8>(p, plan, maps, stream, workspace);
     }
     if (p.residual != nullptr) {

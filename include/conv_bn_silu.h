@@ -173,8 +173,8 @@ int conv_bn_act_forward(const void *x, const void *w, const float *scale, const 
  * from the fp32 epilogue result to the nearest e4m3 (ties to even), saturating
  * to +-448 ("Fusing an Epilogue", section "What an epilogue is": casts to a
  * narrower dtype are epilogue work).  No residual.  The tensor-core path needs
- * c_out % 16 == 0 (16-byte rows) and uses pixel-major tiles; other shapes run
- * on the direct kernel.
+ * c_out % 16 == 0 (16-byte rows) and takes the same tiles as the bf16 layer;
+ * other shapes run on the direct kernel.
  */
 int conv_bn_act_forward_fp8(const void *x, const void *w, const float *scale, const float *bias, void *y,
                             int n, int h, int w_in, int c, int c_out, int r, int s, int stride_h, int stride_w,

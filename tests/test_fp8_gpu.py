@@ -28,7 +28,9 @@ def capi():
 SHAPES = [
     LayerShape("tiny", 1, 32, 32, 16, 32, 3, 3, 1, 1),           # 32-byte fp8 rows (swizzled)
     LayerShape("n16", 2, 17, 19, 16, 16, 3, 3, 2, 1),            # 16-byte fp8 rows
-    LayerShape("down", 2, 80, 80, 64, 128, 3, 3, 2, 1),          # pixel-major although swap would be chosen
+    LayerShape("down", 2, 80, 80, 64, 128, 3, 3, 2, 1),          # pixel-major, 128-wide tiles
+    LayerShape("c2f", 8, 80, 80, 128, 128, 1, 1, 1, 0),          # channel-major (swap AB), balanced 32-pixel runs
+    LayerShape("swapw", 16, 160, 160, 16, 64, 3, 3, 2, 1),       # channel-major, whole 256-pixel tiles
     LayerShape("pairs", 31, 20, 20, 128, 512, 3, 3, 1, 1),       # 2-CTA stream-K
     LayerShape("stem", 1, 64, 64, 3, 16, 3, 3, 2, 1),            # direct kernel
     LayerShape("odd", 1, 9, 7, 16, 24, 3, 3, 1, 1),              # c_out % 16 != 0: direct kernel
