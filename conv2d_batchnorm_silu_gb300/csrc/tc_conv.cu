@@ -1351,7 +1351,13 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
     const long long swap_tiles = ptiles256 * ((p.c_out + kTcBlockM - 1) / kTcBlockM);
     const bool pair_path = p.c_out > 128 && t.k_iters >= 16 && tiles256 >= sm_count;
     const bool short_narrow = p.c_out <= 64 && t.k_iters <= 2;
-    t.swap_ab = (p.c_out >= 32 && p.c_out <= 256 && !pair_path && !short_narrow && swap_tiles >= sm_count / 2)
+    // Fewer swap tiles than half the SMs: balanced runs still spread the pixels over
+    // every SM, and with K loops of eight steps or more their N = 256-wide MMAs beat
+    // the pixel-major tiles (the sweep's 40x40 and 20x20 layers, up to 512 channels).
+    const bool swap_small = p.c_out >= 32 && p.c_out <= 512 && !pair_path && !short_narrow && t.k_iters >= 8 &&
+                            swap_tiles >= sm_count / 4 && swap_tiles < sm_count / 2;
+    t.swap_ab = ((p.c_out >= 32 && p.c_out <= 256 && !pair_path && !short_narrow && swap_tiles >= sm_count / 2) ||
+                 swap_small)
                     ? 1
                     : 0;
     if (q.swap_ab >= 0) t.swap_ab = q.swap_ab ? 1 : 0;
@@ -1375,8 +1381,8 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
         const int grid_bal = (int)std::min<long long>(chunks, sm_count);
         const int grid_whole = std::min(t.tiles, sm_count);
         t.balanced = q.balanced >= 0 ? q.balanced
-                                     : (4 * swap_boxes_balanced(p.m, t.n_tiles, grid_bal) <=
-                                                3 * swap_boxes_whole(t.tiles, grid_whole)
+                                     : (swap_small || 4 * swap_boxes_balanced(p.m, t.n_tiles, grid_bal) <=
+                                                          3 * swap_boxes_whole(t.tiles, grid_whole)
                                             ? 1
                                             : 0);
         t.grid = t.balanced ? grid_bal : grid_whole;

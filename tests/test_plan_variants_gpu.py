@@ -34,8 +34,9 @@ CASES = [
     ("swap_small", LayerShape("ss", 2, 13, 11, 16, 24, 3, 3, 1, 1), {"swap_ab": 1}),
     ("swap_small_tiles", LayerShape("ss", 2, 13, 11, 16, 24, 3, 3, 1, 1), {"swap_ab": 1, "balanced": 0}),
     # balanced runs crossing from the first channel tile into a partial second one
-    ("swap_two_ctiles", LayerShape("bx", 3, 30, 30, 32, 200, 3, 3, 1, 1), {"swap_ab": 1}),
-    ("swap_multi_unit_tail", LayerShape("bl", 5, 37, 29, 64, 136, 3, 3, 1, 1), {"swap_ab": 1}),
+    ("swap_two_ctiles", LayerShape("bx", 3, 30, 30, 32, 200, 1, 1, 1, 0), {"swap_ab": 1}),
+    # two balanced units per CTA (256 pixels and a remainder), a ragged last chunk
+    ("swap_multi_unit_tail", LayerShape("bl", 3, 150, 151, 16, 40, 3, 3, 1, 1), {"balanced": 1}),
     ("pw_swap_tiles", LayerShape("pw", 4, 40, 40, 256, 256, 1, 1, 1, 0), {"swap_ab": 1, "balanced": 0}),
     ("direct", LayerShape("dd", 2, 13, 11, 16, 24, 3, 3, 1, 1), {"algo": "direct"}),
 ]
