@@ -1135,7 +1135,12 @@ std::mutex g_ws_mu;
 Workspace g_ws[64];
 int g_ws_count = 0;
 
-cudaError_t stream_k_workspace(cudaStream_t stream, size_t bytes, size_t flag_bytes, void **out)
+// The buffer is a zeroed flag region followed by the partial tiles.  Plans differ in
+// how many flags they use; every plan's partial tiles start after the buffer's whole
+// flag region (`*flag_region`), so that no plan's partial sums land where another
+// plan's flags live.
+cudaError_t stream_k_workspace(cudaStream_t stream, size_t partial_bytes, size_t flag_bytes, void **out,
+                               size_t *flag_region)
 {
     int device = 0;
     cudaError_t st = cudaGetDevice(&device);
@@ -1144,10 +1149,16 @@ cudaError_t stream_k_workspace(cudaStream_t stream, size_t bytes, size_t flag_by
     Workspace *w = nullptr;
     for (int i = 0; i < g_ws_count; ++i)
         if (g_ws[i].device == device && g_ws[i].stream == stream) w = &g_ws[i];
-    if (w && w->bytes >= bytes && w->flag_bytes >= flag_bytes) {
+    if (w && w->flag_bytes >= flag_bytes && w->bytes - w->flag_bytes >= partial_bytes) {
         *out = w->ptr;
+        *flag_region = w->flag_bytes;
         return cudaSuccess;
     }
+    if (w) {  // grow both parts, never shrink either
+        flag_bytes = std::max(flag_bytes, w->flag_bytes);
+        partial_bytes = std::max(partial_bytes, w->bytes - w->flag_bytes);
+    }
+    const size_t bytes = flag_bytes + partial_bytes;
     if (!w) {
         if (g_ws_count == 64) return cudaErrorMemoryAllocation;
         w = &g_ws[g_ws_count++];
@@ -1171,6 +1182,7 @@ cudaError_t stream_k_workspace(cudaStream_t stream, size_t bytes, size_t flag_by
     w->bytes = bytes;
     w->flag_bytes = flag_bytes;
     *out = ptr;
+    *flag_region = flag_bytes;
     return cudaSuccess;
 }
 
@@ -1221,12 +1233,14 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
     a.chunks_m = (int)((p.m + 31) / 32);
     if (plan.stream_k) {
         void *ws = caller_workspace;
+        size_t flag_region = (size_t)plan.flag_bytes;  // a caller's buffer is laid out as the plan says
         if (ws == nullptr) {
-            st = stream_k_workspace(stream, (size_t)plan.workspace_bytes, (size_t)plan.flag_bytes, &ws);
+            st = stream_k_workspace(stream, (size_t)(plan.workspace_bytes - plan.flag_bytes),
+                                    (size_t)plan.flag_bytes, &ws, &flag_region);
             if (st != cudaSuccess) return st;
         }
         a.flags = static_cast<int *>(ws);
-        a.partial = reinterpret_cast<float *>(static_cast<char *>(ws) + plan.flag_bytes);
+        a.partial = reinterpret_cast<float *>(static_cast<char *>(ws) + flag_region);
     }
     return launch_overlapped(kern, dim3((unsigned)plan.grid), dim3(kTcThreads), (size_t)C::SMEM, stream,
                              PAIR ? 2 : 1, maps.x, maps.w, maps.y, maps.r, a);

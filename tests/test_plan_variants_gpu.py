@@ -85,3 +85,27 @@ def test_balanced_runs_equal_whole_tiles_bitwise(capi, shape):
     torch.cuda.synchronize()
     capi.check()
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
+def test_stream_k_plans_of_different_layouts_share_one_workspace(capi):
+    """The library-held stream-K buffer serves plans of different layouts (2-CTA pairs,
+    single CTAs, 128- and 256-channel tiles: different slot counts and partial-tile sizes)
+    one after another on one stream: no plan's partial sums may land in another plan's
+    flags, and the flags each plan leaves behind are zero."""
+    shape = LayerShape("sk", 31, 20, 20, 128, 512, 3, 3, 1, 1)
+    dev = torch.device("cuda:0")
+    inp = make_layer_inputs(shape, seed=83)
+    x = bits_to_torch_bf16(inp.x_bits).to(dev)
+    w = bits_to_torch_bf16(inp.w_bits).to(dev)
+    g, b, m, v = (torch.from_numpy(a).to(dev) for a in (inp.gamma, inp.beta, inp.mean, inp.var))
+    scale, bias = capi.fold(g, b, m, v, inp.eps)
+    ref = oracle.conv_bn_silu(inp.x_bits, inp.w_bits, inp.gamma, inp.beta, inp.mean, inp.var, inp.eps,
+                              shape.stride, shape.pad)
+    bound = 1e-2 + 1e-2 * np.abs(ref)
+    order = [{}, {"stream_k": 1, "block_n": 128}, {"pair": 0}, {"stream_k": 1, "block_n": 64}, {}]
+    for ov in order * 2:
+        y = capi.forward_request(x, w, scale, bias, shape.stride, shape.pad, **ov)
+        torch.cuda.synchronize()
+        capi.check()
+        got = bf16_bits_to_f32(torch_bf16_to_bits(y)).astype(np.float64)
+        assert np.all(np.abs(got - ref) <= bound), ov
