@@ -1,6 +1,6 @@
 // fold.cu -- BatchNorm fold to one scale and one bias per output channel.
-// ("Fusing an Epilogue", kernels book: batch norm is "a multiply and an add",
-// loaded inside the fused kernel as one scale and one bias per channel.)
+// ("Fusing an Epilogue", kernels book: batch norm reduces to a multiply and an
+// add, loaded inside the fused kernel as one scale and one bias per channel.)
 //   scale = gamma / sqrt(var + eps), bias = beta - mean * scale,
 // evaluated in double precision and rounded once to float.
 #include <cuda_runtime.h>

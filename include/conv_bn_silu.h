@@ -55,9 +55,9 @@ typedef enum cbs_algo {
 /*
  * BatchNorm fold, run once per layer at load time.
  *   scale[k] = gamma[k] / sqrt(var[k] + eps),  bias[k] = beta[k] - mean[k] * scale[k]
- * The fusion page describes BN as "a multiply and an add" with "one scale and
- * one bias per output channel" ("Fusing an Epilogue", sections "The problem"
- * and "The shape of it"); this is the inference-mode fold with running
+ * The fusion page treats BN as one multiply and one add per element, with a
+ * scale and a bias per output channel ("Fusing an Epilogue", sections "The
+ * problem" and "The shape of it"); this is the inference-mode fold with running
  * statistics.  Computed in double precision, rounded once to float.
  *   gamma, beta, mean, var : device, float32 [c_out]
  *   eps                    : >= 0 and finite

@@ -11,8 +11,8 @@ library routines, identities of the mathematics); see each docstring.
 
 What it follows ("Fusing an Epilogue", kernels book):
 
-* section "The problem": conv, then batch norm ("a multiply and an add"),
-  then SiLU = x * sigmoid(x);
+* section "The problem": conv, then batch norm (a per-channel multiply and
+  add), then SiLU = x * sigmoid(x);
 * section "The shape of it": ``acc = acc * bn_scale + bn_bias`` and then
   ``acc = acc * sigmoid(acc)`` applied to the convolution result.
 
@@ -102,9 +102,9 @@ def bn_fold(gamma, beta, mean, var, eps) -> tuple[np.ndarray, np.ndarray]:
     BN(t) = gamma * (t - mean) / sqrt(var + eps) + beta
           = t * scale + bias, with scale = gamma / sqrt(var + eps) and
                                    bias  = beta - mean * scale.
-    The fusion page describes BN as "a multiply and an add" with "one scale
-    and one bias per output channel" (sections "The problem" and "The shape
-    of it") but prints no fold; this is the plainest reading.  float64.
+    The fusion page treats BN as one multiply and one add with a scale and a
+    bias per output channel (sections "The problem" and "The shape of it")
+    but prints no fold; this is the plainest reading.  float64.
     """
     g = np.asarray(gamma, dtype=np.float64)
     b = np.asarray(beta, dtype=np.float64)

@@ -6,7 +6,7 @@
  *
  * What it follows ("Fusing an Epilogue", kernels book):
  *   - section "The problem": the layer is a convolution, then batch
- *     normalisation ("a multiply and an add"), then SiLU, x * sigmoid(x);
+ *     normalisation (a per-channel multiply and add), then SiLU, x * sigmoid(x);
  *   - section "The shape of it": after the K loop the accumulator is scaled
  *     and shifted per output channel (acc * bn_scale + bn_bias) and then
  *     multiplied by its own sigmoid.
