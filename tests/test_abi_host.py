@@ -248,3 +248,22 @@ def test_tuning_sweep_variants_are_consistent():
         assert ov.get("balanced", -1) != 1 or ov["swap_ab"] == 1
     assert len(tune.SWEEP) >= 15 and len({s.name for s in tune.SWEEP}) == len(tune.SWEEP)
 
+
+
+def test_planner_choices_match_the_measured_sweep():
+    """The planner's choice for every layer of the threshold sweep, as measured on a GB300
+    (152 SMs) and recorded with the sweep's timings: a change to the planner's rules changes
+    one of these and calls for the sweep to be run again."""
+    from conv2d_batchnorm_silu_gb300 import capi, tune
+    expected = {
+        "stem640": "thin-input", "down320": "swap-tiles", "c2f160_1x1": "n64", "bneck160": "swap-tiles",
+        "down160": "swap", "c2f80_1x1": "swap", "bneck80": "swap", "down80": "swap-tiles",
+        "c2f40_1x1": "swap-tiles", "bneck40": "swap", "down40": "swap", "c2f20_1x1": "swap",
+        "bneck20": "n128", "sppf20_1x1": "n128", "head80_3x3": "swap", "tiny": "n32",
+        "stem": "thin-input", "down": "swap-tiles", "pointwise": "swap", "deep": "n256-sk-pair",
+    }
+    got = {}
+    for sh in tune.SWEEP:
+        p = capi.plan(sh.n, sh.h, sh.w, sh.c, sh.k, sh.r, sh.s, sh.stride, sh.pad, "auto", 152)
+        got[sh.name] = tune._plan_label(p)
+    assert got == expected
