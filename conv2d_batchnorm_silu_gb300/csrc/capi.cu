@@ -117,6 +117,8 @@ int launch_forward(const cbs::ConvProblem &p, int algo, cudaStream_t strm, const
         }
         cbs::TcPlan plan{};
         if (cbs::tc_make_plan_request(p, sms, rq, &plan) != 0) return CBS_ERR_UNSUPPORTED;
+        // A stream-K plan needs the library-held workspace of this (device, stream).
+        if (plan.stream_k && !cbs::tc_workspace_reserve(strm)) return CBS_ERR_UNSUPPORTED;
         cudaError_t e = cbs::tc_launch(p, plan, strm);
         return e == cudaSuccess ? CBS_OK : cuda_fail(e);
     }
@@ -192,6 +194,10 @@ int conv_bn_silu_forward_noalloc(const void *x, const void *w, const float *scal
     p.bias = bias;
     p.y = y;
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    // Set-up, on the first call on each device: the scratch array's device address.
+    void *scratch = nullptr;
+    st = noalloc_scratch_address(&scratch);
+    if (st != CBS_OK) return st;
     int sms = 0;
     if (!cbs::tc_supported(p)) {  // neither of these kernels needs scratch
         cudaError_t e;
@@ -206,15 +212,19 @@ int conv_bn_silu_forward_noalloc(const void *x, const void *w, const float *scal
     }
     st = sm_count_current_device(&sms);
     if (st != CBS_OK) return st;
-    const cbs::TcPlan plan = cbs::tc_make_plan(p, sms);
-    void *scratch = nullptr;
+    cbs::TcPlan plan = cbs::tc_make_plan(p, sms);
+    if (plan.stream_k && plan.workspace_bytes > (long long)kNoAllocScratchBytes) {
+        // The split would not fit the array (a GPU with many more SMs than GB300's 152):
+        // whole tiles per CTA instead, which need no scratch.
+        const cbs::PlanRequest whole{-1, 0, 0, 0, -1};
+        if (cbs::tc_make_plan_request(p, sms, &whole, &plan) != 0) return CBS_ERR_UNSUPPORTED;
+    }
     if (plan.stream_k) {
-        if (plan.workspace_bytes > (long long)kNoAllocScratchBytes) return CBS_ERR_UNSUPPORTED;
-        st = noalloc_scratch_address(&scratch);
-        if (st != CBS_OK) return st;
         // The ready flags must start at zero; a previous call that gave up may have left some set.
         cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)plan.flag_bytes, strm);
         if (e != cudaSuccess) return cuda_fail(e);
+    } else {
+        scratch = nullptr;
     }
     cudaError_t e = cbs::tc_launch_with_workspace(p, plan, strm, scratch);
     return e == cudaSuccess ? CBS_OK : cuda_fail(e);

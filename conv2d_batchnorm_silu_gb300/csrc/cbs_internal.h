@@ -154,6 +154,11 @@ constexpr int kGatherBlockThreads = 288;
 
 // Device error words (one per kernel translation unit): read and clear, stream-ordered.
 cudaError_t tc_read_and_clear_error(cudaStream_t stream, unsigned int *out);
+// Library-held stream-K workspaces: one per (device, stream), at most this many.
+constexpr int kWorkspaceStreams = 64;
+// Makes sure the current device and `stream` have an entry in the workspace table
+// (created empty when missing); false when the table is full.
+bool tc_workspace_reserve(cudaStream_t stream);
 // Re-zeroes the stream-K ready flags of every workspace the library holds (after a
 // kernel gave up mid-way, flags may be left raised).  Synchronous.
 cudaError_t tc_reset_workspaces();

@@ -111,19 +111,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
         : "memory");
 }
 
-// Tiled 3-D load multicast to every CTA of the cluster in `cta_mask`: the data
-// lands at the same shared-memory offset in each, and each one's mbarrier at
-// offset `bar` receives the byte count.
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap *tm, uint32_t bar,
-                                                      int c0, int c1, int c2, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
-        : "memory");
-}
-
 // Tiled 3-D load issued by either CTA of a 2-CTA pair (tcgen05 cta_group::2):
 // the data lands in this CTA's shared memory at `dst`, and the byte count
 // completes on the mbarrier at shared::cluster address `bar_cluster`, which
@@ -199,7 +186,6 @@ __device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const CUtensorM
         : "memory");
 }
 
-// Tiled 2-D store from shared memory (elements outside the tensor are skipped).
 // Tiled 2-D load into shared memory, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, uint32_t bar, int c0, int c1)
 {
@@ -210,6 +196,7 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
         : "memory");
 }
 
+// Tiled 2-D store from shared memory (elements outside the tensor are skipped).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, uint32_t src, int c0, int c1)
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

@@ -1132,7 +1132,7 @@ struct Workspace {
     size_t bytes, flag_bytes;
 };
 std::mutex g_ws_mu;
-Workspace g_ws[64];
+Workspace g_ws[kWorkspaceStreams];
 int g_ws_count = 0;
 
 // The buffer is a zeroed flag region followed by the partial tiles.  Plans differ in
@@ -1149,7 +1149,7 @@ cudaError_t stream_k_workspace(cudaStream_t stream, size_t partial_bytes, size_t
     Workspace *w = nullptr;
     for (int i = 0; i < g_ws_count; ++i)
         if (g_ws[i].device == device && g_ws[i].stream == stream) w = &g_ws[i];
-    if (w && w->flag_bytes >= flag_bytes && w->bytes - w->flag_bytes >= partial_bytes) {
+    if (w && w->ptr && w->flag_bytes >= flag_bytes && w->bytes - w->flag_bytes >= partial_bytes) {
         *out = w->ptr;
         *flag_region = w->flag_bytes;
         return cudaSuccess;
@@ -1160,7 +1160,7 @@ cudaError_t stream_k_workspace(cudaStream_t stream, size_t partial_bytes, size_t
     }
     const size_t bytes = flag_bytes + partial_bytes;
     if (!w) {
-        if (g_ws_count == 64) return cudaErrorMemoryAllocation;
+        if (g_ws_count == kWorkspaceStreams) return cudaErrorMemoryAllocation;  // tc_workspace_reserve said no
         w = &g_ws[g_ws_count++];
         *w = Workspace{device, stream, nullptr, 0, 0};
     } else if (w->ptr) {
@@ -1457,6 +1457,18 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
     }
     *out = t;
     return 0;
+}
+
+bool tc_workspace_reserve(cudaStream_t stream)
+{
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    for (int i = 0; i < g_ws_count; ++i)
+        if (g_ws[i].device == device && g_ws[i].stream == stream) return true;
+    if (g_ws_count == kWorkspaceStreams) return false;
+    g_ws[g_ws_count++] = Workspace{device, stream, nullptr, 0, 0};
+    return true;
 }
 
 TcPlan tc_make_plan(const ConvProblem &p, int sm_count)

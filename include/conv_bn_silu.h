@@ -89,9 +89,9 @@ int conv_bn_silu_fold_batch(const cbs_fold_layer *layers, int n_layers, void *st
 /*
  * Fused forward pass: y = SiLU(conv2d(x, W) * scale + bias).
  * ("Fusing an Epilogue", section "The shape of it": the K loop accumulates
- * the output tile, then acc = acc*bn_scale + bn_bias, acc = acc*sigmoid(acc),
- * then one store; section "Three kernels for one operation": convolution as
- * a GEMM on the tensor cores.)
+ * the output tile; while it is still on chip, a per-channel multiply-add
+ * and then SiLU are applied, and the tile is stored once; section "Three
+ * kernels for one operation": convolution as a GEMM on the tensor cores.)
  *   x     : device, bf16 NHWC [n][h][w_in][c]
  *   w     : device, bf16 KRSC [c_out][r][s][c]
  *   scale : device, float32 [c_out]  (from conv_bn_silu_fold, or any per-channel multiplier)
@@ -101,7 +101,25 @@ int conv_bn_silu_fold_batch(const cbs_fold_layer *layers, int n_layers, void *st
  * no-op.  The result is bf16 rounded to nearest even from an fp32
  * accumulator; it is deterministic (no atomics, fixed reduction order).
  * Kernels: the tcgen05 implicit GEMM when c % 16 == 0 and c_out % 8 == 0,
+ * the thin-input tcgen05 kernel for 3x3 filters over 1, 3 or 4 channels,
  * otherwise the CUDA-core direct kernel.
+ * Host work and memory held by the library, which this and every other
+ * forward entry point (except conv_bn_silu_forward_noalloc) may do:
+ *   - The first call of a shape on a set of buffers encodes TMA descriptors
+ *     (host driver calls; cached for later calls), and the first launch of a
+ *     kernel on a device sets its shared-memory limit.
+ *   - Plans that split K loops between CTAs (cbs_plan_info.stream_k == 1,
+ *     e.g. the 32x20x20x512 -> 512 3x3 layer) keep fp32 partial tiles in a
+ *     scratch buffer the library holds, one per (device, stream).  The first
+ *     such call on a stream allocates it with cudaMalloc (an implicit device
+ *     synchronisation) and zeroes its flags with cudaMemsetAsync on `stream`;
+ *     a later call that needs a larger buffer first synchronises `stream`,
+ *     frees the old buffer and allocates a new one.  The buffers are kept
+ *     until the process exits.  Make each such shape's first call on a stream
+ *     before capturing that stream into a CUDA graph.
+ *   - At most 64 (device, stream) pairs can hold such a buffer: a stream-K
+ *     call on a 65th returns CBS_ERR_UNSUPPORTED (nothing is launched).
+ *     conv_bn_silu_forward_noalloc needs none of this.
  */
 int conv_bn_silu_forward(const void *x, const void *w, const float *scale, const float *bias,
                          void *y, int n, int h, int w_in, int c, int c_out, int r, int s,
@@ -121,11 +139,15 @@ int conv_bn_silu_forward_algo(const void *x, const void *w, const float *scale, 
  * cudaMalloc's implicit synchronisation is not acceptable, or hosts that hand
  * out only pre-sized buffers.  The fusion page has no counterpart to this; it
  * is a deployment convenience of this library.
- * Same arguments, layouts, results and errors as conv_bn_silu_forward.  Where
- * the plan splits K loops between CTAs (stream-K), the partial tiles go to a
- * fixed 20 MiB device array inside the library instead of a library-allocated
- * buffer: shapes whose split needs more (see cbs_plan_info.workspace_bytes)
- * return CBS_ERR_UNSUPPORTED.  Nothing is allocated by any call.
+ * Same arguments, layouts, results and errors as conv_bn_silu_forward, and
+ * the same plan: where the plan splits K loops between CTAs (stream-K), the
+ * partial tiles go to a fixed 20 MiB device array inside the library instead
+ * of a library-allocated buffer, so the result is bit-identical to
+ * conv_bn_silu_forward's.  A split that would need more than 20 MiB (see
+ * cbs_plan_info.workspace_bytes; on a 152-SM GB300 every split fits) runs
+ * whole tiles per CTA instead, which need no scratch: same values within the
+ * layer's tolerance, not necessarily bit-identical.  Nothing is allocated by
+ * any call, and no memory is held per stream.
  *   - The first call on a device looks up that array's device address (once
  *     per device, with that device current); make that first call before any
  *     stream capture.

@@ -13,8 +13,9 @@ What it follows ("Fusing an Epilogue", kernels book):
 
 * section "The problem": conv, then batch norm (a per-channel multiply and
   add), then SiLU = x * sigmoid(x);
-* section "The shape of it": ``acc = acc * bn_scale + bn_bias`` and then
-  ``acc = acc * sigmoid(acc)`` applied to the convolution result.
+* section "The shape of it": the convolution's accumulated result is first
+  multiplied by a per-channel scale and offset by a per-channel bias, and the
+  sum is then multiplied by its own sigmoid.
 
 Readings where the page is silent (each one listed with the others in the
 design notes): inference-mode BatchNorm with running statistics folded to a

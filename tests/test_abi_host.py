@@ -129,6 +129,18 @@ def test_invalid_arguments_return_status_without_gpu(lib):
              None) == lib.CBS_OK
     assert f("conv_bn_silu_forward", None, None, None, None, None, 2, 8, 8, 16, 0, 3, 3, 1, 1, 1, 1,
              None) == lib.CBS_OK
+    # allocation-free forward: validated like conv_bn_silu_forward, before any CUDA call
+    na = "conv_bn_silu_forward_noalloc"
+    for nulls in [(None, good, good, good, good), (good, None, good, good, good),
+                  (good, good, None, good, good), (good, good, good, None, good),
+                  (good, good, good, good, None)]:
+        assert f(na, *nulls, 1, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1, None) == lib.CBS_ERR_INVALID_ARG
+    for odds in [(odd, good, good, good, good), (good, good, good, good, odd)]:
+        assert f(na, *odds, 1, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1, None) == lib.CBS_ERR_MISALIGNED
+    assert f(na, good, good, good, good, good, 1, 8, 8, 16, 16, 3, 3, 0, 1, 1, 1, None) == \
+        lib.CBS_ERR_INVALID_ARG
+    assert f(na, None, None, None, None, None, 0, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1, None) == lib.CBS_OK
+    assert f(na, None, None, None, None, None, 2, 8, 8, 16, 0, 3, 3, 1, 1, 1, 1, None) == lib.CBS_OK
     # unfused comparator: t1/t2 are checked like y
     uf = "conv_bn_silu_forward_unfused"
     dims = (1, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1)
@@ -267,3 +279,23 @@ def test_planner_choices_match_the_measured_sweep():
         p = capi.plan(sh.n, sh.h, sh.w, sh.c, sh.k, sh.r, sh.s, sh.stride, sh.pad, "auto", 152)
         got[sh.name] = tune._plan_label(p)
     assert got == expected
+
+
+def test_noalloc_fallback_plan_needs_no_scratch(lib):
+    """conv_bn_silu_forward_noalloc holds 20 MiB of stream-K scratch.  On a 152-SM GB300
+    every stream-K split fits; with more SMs a split can need more, and the entry point
+    then runs the whole-tile plan (stream_k = 0, pair = 0), which must exist and need none."""
+    cap = 20 << 20
+    deep = (32, 20, 20, 512, 512, 3, 3, 1, 1)
+    split244 = (39, 20, 20, 256, 384, 3, 3, 1, 1)
+    for shape in (deep, split244):
+        assert lib.plan_request(*shape, sm_count=152)["workspace_bytes"] <= cap
+    over = 0
+    for sms in (160, 170, 188, 200):
+        for shape in (deep, split244):
+            p = lib.plan_request(*shape, sm_count=sms)
+            if p["stream_k"] and p["workspace_bytes"] > cap:
+                over += 1
+                q = lib.plan_request(*shape, sm_count=sms, stream_k=0, pair=0)
+                assert q["stream_k"] == 0 and q["cluster"] == 1 and q["workspace_bytes"] == 0
+    assert over > 0   # the fallback is reachable on some larger GPU

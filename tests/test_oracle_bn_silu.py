@@ -1,8 +1,8 @@
 """Pins for the oracle's BN fold, its SiLU and the whole composed layer (CPU only).
 
 "Fusing an Epilogue", sections "The problem" and "The shape of it": batch
-norm is a per-channel multiply and add (``acc * bn_scale + bn_bias``) and
-SiLU is ``x * sigmoid(x)``.  The page prints no values, so these pins use
+norm is a per-channel multiply and add on the convolution's result, and
+SiLU multiplies a value by its sigmoid.  The page prints no values, so these pins use
 exact hand-made fold cases (tests/golden), closed forms of SiLU, and values
 from mpmath at 50 digits, an arbitrary-precision library independent of
 numpy's exp.
