@@ -60,6 +60,7 @@ WORKLOAD = ("five YOLO-shaped fused conv+BN+SiLU layers per step: one batched BN
             "deep 32x20x20x512->512 3x3s1p1; NHWC bf16 x, KRSC bf16 W, fp32 BN")
 DOMINANT = "deep"
 ROTATION = 3
+CLOCK_WINDOW_S = 1.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CLOCK_FIELDS = ("timestamp,uuid,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -88,6 +89,9 @@ def parse_args(argv=None):
                     help="graph replays for the back-to-back per-layer times (0: skip)")
     ap.add_argument("--no-gemm-context", action="store_true",
                     help="skip timing cuBLAS on plain GEMMs of the pointwise and deep layers' sizes")
+    ap.add_argument("--clock-window-s", type=float, default=CLOCK_WINDOW_S,
+                    help="seconds of the same step replayed right after the timed steps, inside the "
+                         "clock record (0: the timed steps alone)")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch through the API each step instead of replaying CUDA graphs")
     args = ap.parse_args(argv)
@@ -142,7 +146,7 @@ def load_peaks() -> tuple[dict, str]:
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
 
-    def __init__(self, uuid: str | None, interval_ms: int = 100):
+    def __init__(self, uuid: str | None, interval_ms: int = 50):
         self.uuid = uuid
         self.proc = None
         try:
@@ -349,15 +353,32 @@ def run_ours(args, rank, world, local_rank):
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
+    torch.cuda.nvtx.range_push("timed steps")
     with torch.cuda.stream(stream):
         start.record(stream)
         for i in range(K):
             step(i, None if dom_ev is None else (dom_ev[0][i], dom_ev[1][i]))
         end.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    # The clock record covers the timed steps and the same step replayed for
+    # CLOCK_WINDOW_S more seconds right after them, so that a short timed region
+    # (--steps 20 lasts about 2 ms) still has nvidia-smi samples under the same load.
+    torch.cuda.nvtx.range_push("clock window")
+    with torch.cuda.stream(stream):
+        i = 0
+        while time.time() - t_wall0 < args.clock_window_s:
+            for _ in range(200):
+                step(i)
+                i += 1
+            torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     t_wall1 = time.time()
     barrier(world)
     clocks = sampler.stop(t_wall0, t_wall1)
+    if clocks is not None:
+        clocks["window"] = (f"the timed steps plus the same step replayed right after them, "
+                            f"{t_wall1 - t_wall0:.2f} s in all, sampled every 50 ms")
     capi.check(stream)
     elapsed_s = start.elapsed_time(end) / 1e3
     elapsed_max = max_over_ranks(elapsed_s, world, dev)
@@ -371,7 +392,10 @@ def run_ours(args, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     b2b = layer_times_back_to_back(capi, sets, inputs, layers, stream, dev,
                                    args.b2b_replays) if args.b2b_replays > 0 else None
+    torch.cuda.nvtx.range_push("per-layer timings")
     iso = isolated_layer_times(capi, sets, layers, stream, dev, args.iso_iters)
+    iso_clean = isolated_layer_times(capi, sets, layers, stream, dev, args.iso_iters, clean=True)
+    torch.cuda.nvtx.range_pop()
     per_layer = {}
     for n in layers:
         sh = LAYERS[n]
@@ -380,6 +404,8 @@ def run_ours(args, rank, world, local_rank):
         t_byte = sh.compulsory_bytes / (peaks["hbm_gbs"] * 1e9)
         pl = capi.plan(sh.n, sh.h, sh.w, sh.c, sh.k, sh.r, sh.s, sh.stride, sh.pad)
         per_layer[n] = {"us_per_call": round(iso[n], 3),
+                        "us_per_call_clean_l2": round(iso_clean[n], 3),
+                        "roofline_frac_clean_l2": round(max(t_flop, t_byte) / (iso_clean[n] * 1e-6), 4),
                         "tflops": round(sh.flops / t / 1e12, 2),
                         "gbs": round(sh.compulsory_bytes / t / 1e9, 1),
                         "roofline_us": round(max(t_flop, t_byte) * 1e6, 3),
@@ -438,10 +464,16 @@ def run_ours(args, rank, world, local_rank):
                               "one CUDA graph per step captured from the API calls, replayed"),
                    "parallelism": f"replicas x{world} (each rank runs the full step)"},
         "roofline": roofline,
+        "layers_roofline_frac": {n: {"isolated": per_layer[n]["roofline_frac"],
+                                     "isolated_clean_l2": per_layer[n].get("roofline_frac_clean_l2"),
+                                     "back_to_back": per_layer[n].get("roofline_frac_back_to_back")}
+                                 for n in layers},
         "per_layer": per_layer,
         "per_layer_timing": {
             "us_per_call": "median of isolated calls, a 512 MB L2-flushing write before each; "
                            "includes the launch gap of a lone call",
+            "us_per_call_clean_l2": "as us_per_call, with a 512 MB read after the flushing write, so the "
+                                    "flush's dirty lines are written back before the call, not during it",
             "us_back_to_back": (None if b2b is None else
                                 "one CUDA graph of G forwards of the layer back to back, each on its own "
                                 "buffer set (rotation > 160 MB unless marked l2_resident), replayed "
@@ -625,10 +657,15 @@ def gemm_context(dev, layers, fused_us, iters) -> dict:
     return {"layers": out, "note": "cuBLAS on the same-size plain GEMM without BN/SiLU; context only"}
 
 
-def isolated_layer_times(capi, sets, layers, stream, dev, iters) -> dict:
+def isolated_layer_times(capi, sets, layers, stream, dev, iters, clean=False) -> dict:
     """Median forward time of each layer alone: the L2 is flushed (a 512 MB write) before
-    every call and CUDA events on the stream bracket the forward kernel only."""
+    every call and CUDA events on the stream bracket the forward kernel only.
+
+    clean=True: the write is followed by a read of another 512 MB buffer, so that the
+    flush's own dirty lines are written back before the call instead of during it (the L2
+    the call starts with then holds only clean lines of an unrelated buffer)."""
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(128 * 1024 * 1024, dtype=torch.float32, device=dev) if clean else None
     out = {}
     with torch.cuda.stream(stream):
         for n in layers:
@@ -637,6 +674,8 @@ def isolated_layer_times(capi, sets, layers, stream, dev, iters) -> dict:
                 lb = sets[i % ROTATION][n]
                 sh = lb.shape
                 flush.zero_()
+                if clean:
+                    flush_r.sum()
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -645,7 +684,7 @@ def isolated_layer_times(capi, sets, layers, stream, dev, iters) -> dict:
                 evs.append((a, b))
             torch.cuda.synchronize()
             out[n] = 1e3 * statistics.median(a.elapsed_time(b) for a, b in evs)
-    del flush
+    del flush, flush_r
     return out
 
 
@@ -846,6 +885,31 @@ def sample_pixels(fraction: float, inputs, seed: int = 0) -> dict:
     return out
 
 
+def cpu_model() -> str:
+    """The host CPU's model name: lscpu's "Model name" (Arm hosts have no "model name" line in
+    /proc/cpuinfo), else /proc/cpuinfo's, else its implementer/part codes."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        names = [ln.split(":", 1)[1].strip() for ln in out.splitlines() if ln.startswith("Model name:")]
+        vendor = [ln.split(":", 1)[1].strip() for ln in out.splitlines() if ln.startswith("Vendor ID:")]
+        if names:
+            return " ".join(vendor[:1] + names[:1])
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ":" in ln:
+                    k, v = ln.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+        if "model name" in fields:
+            return fields["model name"]
+        return f"CPU implementer {fields.get('CPU implementer', '?')} part {fields.get('CPU part', '?')}"
+    except OSError:
+        return "unknown"
+
+
 def cpu_baseline(seconds: float, layers=LAYER_ORDER) -> dict:
     """The oracle as it stands, on this host's cores, over a bounded sample of the workload.
 
@@ -864,7 +928,7 @@ def cpu_baseline(seconds: float, layers=LAYER_ORDER) -> dict:
             break
         frac = min(1.0, frac * max(2.0, min(8.0, seconds / max(dt, 1e-3) / 2)))
     return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": oracle.default_threads(),
-            "kind": "oracle",
+            "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"{frac:.3g} of every layer's output pixels (evenly spaced, all channels), "
                       f"{sum(p.size for p in pix.values())} pixels, {flops / 1e9:.2f} GFLOP in {dt:.1f} s"}
 
@@ -902,7 +966,7 @@ def run_reference(args, rank, world):
         "config": {"workload": WORKLOAD, "l2": "n/a (CPU)", "parallelism": "host threads"},
         "impl": "reference",
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": oracle.default_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

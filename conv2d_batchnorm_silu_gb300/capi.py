@@ -43,7 +43,9 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in (
         "algo", "block_m", "block_n", "block_k", "stages", "tiles", "grid", "threads",
         "smem_bytes", "k_iters", "stream_k", "swap_ab", "cluster")] + [("workspace_bytes", ctypes.c_longlong),
-                                                                        ("balanced", ctypes.c_int)]
+                                                                        ("balanced", ctypes.c_int),
+                                                                        ("weights_resident", ctypes.c_int),
+                                                                        ("row_boxes", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         d = {name: getattr(self, name) for name, _ in self._fields_}
@@ -61,13 +63,14 @@ class PlanRequest(ctypes.Structure):
     """cbs_plan_request: overrides of the planner's choices (-1 / 0: planner's choice) and the
     bound on the tcgen05 kernel's pipeline waits (0: the 2 s default)."""
     _fields_ = [(name, ctypes.c_int) for name in ("algo", "swap_ab", "stream_k", "pair", "block_n")] + \
-        [("wait_timeout_ns", ctypes.c_longlong), ("balanced", ctypes.c_int)]
+        [("wait_timeout_ns", ctypes.c_longlong), ("balanced", ctypes.c_int), ("weights_resident", ctypes.c_int),
+         ("row_boxes", ctypes.c_int)]
 
 
 def _request(algo="auto", swap_ab=-1, stream_k=-1, pair=-1, block_n=0, wait_timeout_ns=0,
-             balanced=-1) -> PlanRequest:
+             balanced=-1, weights_resident=-1, row_boxes=-1) -> PlanRequest:
     return PlanRequest(ALGOS[algo], int(swap_ab), int(stream_k), int(pair), int(block_n), int(wait_timeout_ns),
-                       int(balanced))
+                       int(balanced), int(weights_resident), int(row_boxes))
 
 
 def _declare(name, argtypes, restype=ctypes.c_int):

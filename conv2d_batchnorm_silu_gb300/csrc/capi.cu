@@ -98,7 +98,7 @@ int sm_count_current_device(int *count)
 bool has_overrides(const cbs::PlanRequest *rq)
 {
     return rq && (rq->swap_ab >= 0 || rq->stream_k >= 0 || rq->pair >= 0 || rq->block_n != 0 ||
-                  rq->balanced >= 0);
+                  rq->balanced >= 0 || rq->wres >= 0 || rq->row_boxes >= 0);
 }
 
 // Validated problem (pointers set) -> the chosen kernel's launch on `strm`.
@@ -133,13 +133,14 @@ int read_request(const cbs_plan_request *req, int *algo, cbs::PlanRequest *rq)
     if (!req) return CBS_ERR_INVALID_ARG;
     if (req->wait_timeout_ns < 0) return CBS_ERR_INVALID_ARG;
     if (req->algo < CBS_ALGO_AUTO || req->algo > CBS_ALGO_DIRECT) return CBS_ERR_INVALID_ARG;
-    for (int v : {req->swap_ab, req->stream_k, req->pair, req->balanced})
+    for (int v : {req->swap_ab, req->stream_k, req->pair, req->balanced, req->weights_resident, req->row_boxes})
         if (v < -1 || v > 1) return CBS_ERR_INVALID_ARG;
     if (req->block_n != 0 && req->block_n != 16 && req->block_n != 32 && req->block_n != 64 &&
         req->block_n != 128 && req->block_n != 256)
         return CBS_ERR_INVALID_ARG;
     *algo = req->algo;
-    *rq = cbs::PlanRequest{req->swap_ab, req->stream_k, req->pair, req->block_n, req->balanced};
+    *rq = cbs::PlanRequest{req->swap_ab, req->stream_k, req->pair, req->block_n, req->balanced,
+                           req->weights_resident, req->row_boxes};
     return CBS_OK;
 }
 
@@ -216,7 +217,7 @@ int conv_bn_silu_forward_noalloc(const void *x, const void *w, const float *scal
     if (plan.stream_k && plan.workspace_bytes > (long long)kNoAllocScratchBytes) {
         // The split would not fit the array (a GPU with many more SMs than GB300's 152):
         // whole tiles per CTA instead, which need no scratch.
-        const cbs::PlanRequest whole{-1, 0, 0, 0, -1};
+        const cbs::PlanRequest whole{-1, 0, 0, 0, -1, -1, -1};
         if (cbs::tc_make_plan_request(p, sms, &whole, &plan) != 0) return CBS_ERR_UNSUPPORTED;
     }
     if (plan.stream_k) {
@@ -417,25 +418,24 @@ static int fill_plan(const cbs::ConvProblem &p, int algo, int sm_count, const cb
     cbs_plan_info out{};
     out.algo = chosen;
     if (chosen == CBS_ALGO_TCGEN05 && !cbs::tc_supported(p)) {
-        if (!cbs::gather_supported(p) || has_overrides(rq)) return CBS_ERR_UNSUPPORTED;
-        // Thin-input kernel: one 128-pixel tile per MMA step, K zero-padded to 32 or 64.
-        const int taps = r * s * c;
-        const int n16 = (c_out + 15) / 16 * 16;
-        const long long tiles = (p.m + 127) / 128;
+        // Thin-input kernel: 128-pixel tiles, K zero-padded to 32 or 64, each CTA an equal
+        // range of pixels whose input rows it stages in shared memory.
+        cbs::GatherPlan g{};
+        if (has_overrides(rq) || !cbs::gather_plan(p, sm_count, &g)) return CBS_ERR_UNSUPPORTED;
         out.block_m = 128;
-        out.block_n = n16;
-        out.block_k = taps <= 32 ? 32 : 64;
-        out.stages = 4;
-        out.tiles = (int)tiles;
-        out.grid = (int)(tiles < 2LL * sm_count ? tiles : 2LL * sm_count);
+        out.block_n = g.block_n;
+        out.block_k = g.block_k;
+        out.stages = g.stages;
+        out.tiles = g.tiles;
+        out.grid = g.grid;
         out.threads = cbs::kGatherBlockThreads;
-        out.smem_bytes = 1024 + 4 * 128 * out.block_k * 2 + (n16 * out.block_k * 2 + 1023) / 1024 * 1024 + 256;
+        out.smem_bytes = g.smem_bytes;
         out.k_iters = 1;
         out.cluster = 1;
     } else if (chosen == CBS_ALGO_TCGEN05) {
         cbs::TcPlan t{};
         if (cbs::tc_make_plan_request(p, sm_count, rq, &t) != 0) return CBS_ERR_UNSUPPORTED;
-        out.block_m = t.swap_ab ? t.block_n : cbs::kTcBlockM;  // output pixels per tile
+        out.block_m = t.cmajor ? t.cm_unit_px : (t.swap_ab ? t.block_n : cbs::kTcBlockM);  // output pixels per tile
         out.block_n = t.swap_ab ? cbs::kTcBlockM : t.block_n;  // output channels per tile
         out.block_k = t.block_k;
         out.stages = t.stages;
@@ -449,6 +449,8 @@ static int fill_plan(const cbs::ConvProblem &p, int algo, int sm_count, const cb
         out.cluster = t.pair ? 2 : 1;
         out.workspace_bytes = t.workspace_bytes;
         out.balanced = t.balanced;
+        out.weights_resident = t.cmajor ? t.cm_wres : 0;
+        out.row_boxes = t.cmajor && t.cm_xmode != 0 ? 1 : 0;
     } else {
         if (has_overrides(rq)) return CBS_ERR_UNSUPPORTED;  // the direct kernel has no tilings to choose
         const long long bx = (p.m + cbs::kDirectThreads - 1) / cbs::kDirectThreads;
@@ -526,7 +528,10 @@ int conv_bn_silu_check(void *stream)
     unsigned int gword = 0;
     e = cbs::gather_read_and_clear_error(static_cast<cudaStream_t>(stream), &gword);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (gword != 0 && word == 0) return CBS_ERR_TIMEOUT;
+    unsigned int wword = 0;
+    e = cbs::cmajor_read_and_clear_error(static_cast<cudaStream_t>(stream), &wword);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if ((gword != 0 || wword != 0) && word == 0) return CBS_ERR_TIMEOUT;
     if (word == 0) return CBS_OK;
     // A kernel gave up mid-way: stream-K ready flags may be left raised.
     e = cbs::tc_reset_workspaces();

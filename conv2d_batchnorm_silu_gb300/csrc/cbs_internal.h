@@ -2,6 +2,7 @@
 // translation units.  Not part of the public interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -49,13 +50,23 @@ struct TcPlan {
     int balanced;                 // swap_ab only: each CTA takes an equal run of 32-pixel chunks (see tc_conv.cu)
     long long workspace_bytes;    // stream-K partial tiles + flags (0 when not split)
     long long flag_bytes;         // the leading part of the workspace that must start zeroed
+    // The channel-major kernel of tc_cmajor.cu (cmajor = 1): units of cm_unit_px pixels,
+    // x in boxes of cm_unit_rows whole output rows (0: im2col boxes), the weight tile
+    // resident in tensor memory (cm_wres = 1) or loaded with every K step.
+    int cmajor;
+    int cm_wres;
+    int cm_xmode;                 // 0 im2col boxes, 1 row boxes, 2 boxes of the [M][C] matrix (1x1, stride 1)
+    int cm_unit_px;
+    int cm_unit_rows;
+    int cm_ctas_per_tile;         // CTAs per 128-channel tile (the grid is this x channel tiles)
+    int cm_stage_bytes;           // one pipeline stage
+    int cm_a_bytes;               // streamed weights: the weight part of a stage
 };
 
 constexpr int kTcBlockM = 128;
 constexpr int kTcThreads = 384;  // producer, MMA, two idle, eight epilogue warps
-// Stream-K slot words: a ready flag per epilogue warp, then an arrival ticket per epilogue warp.
-constexpr int kTcFlagsPerSlot = 16;
-constexpr int kTcTicketOffset = 8;
+// Stream-K slot words: a ready flag per epilogue warp.
+constexpr int kTcFlagsPerSlot = 8;
 
 // Epilogue geometry of the tensor-core kernel for an N tile of `block_n`
 // channels: `split` warps share each 32-row TMEM lane quarter (each takes
@@ -107,10 +118,28 @@ TcPlan tc_make_plan(const ConvProblem &p, int sm_count);
 struct PlanRequest {
     int swap_ab, stream_k, pair, block_n;
     int balanced;  // channel-major tiles: -1 planner, 0 whole 256-pixel tiles, 1 equal runs of 32-pixel chunks
+    int wres;      // -1 planner, 0 weights streamed with every tile, 1 weights resident in tensor memory
+    int row_boxes; // -1 planner, 0 im2col boxes, 1 boxes of whole output rows (channel-major kernel)
 };
 // As tc_make_plan with the overrides in `rq` (nullable); -1 when the kernel cannot run
 // them on this shape (e.g. stream-K shares shorter than one tile).
 int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *rq, TcPlan *out);
+// The channel-major kernel's plan (tc_cmajor.cu) with the weights resident in tensor memory
+// or not and x in row boxes or im2col boxes; false when it cannot run that combination.
+bool cmajor_fill_plan(const ConvProblem &p, int sm_count, int wres, int xrows, TcPlan *t);
+cudaError_t cmajor_launch(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream);
+cudaError_t cmajor_read_and_clear_error(cudaStream_t stream, unsigned int *out);
+// Tensor maps shared by the tensor-core kernels (tc_conv.cu): x in im2col mode with boxes
+// of `box_pixels` output pixels x block_k channels; a weight load of block_k channels of
+// one filter tap for `rows` output channels; a tensor shaped like y, unswizzled boxes.
+cudaError_t tc_encode_x_im2col(const ConvProblem &p, int block_k, int box_pixels, CUtensorMap *out);
+// x viewed as (stride*C, W/stride, H, N) with boxes of block_k channels x wo view pixels x
+// `rows` input rows taken every stride-th row (W divisible by the stride).
+cudaError_t tc_encode_x_rows(const ConvProblem &p, int block_k, int rows, CUtensorMap *out);
+// x of a 1x1 stride-1 layer as the [M][C] matrix, boxes of block_k channels x box_rows pixels.
+cudaError_t tc_encode_x_matrix(const ConvProblem &p, int block_k, int box_rows, CUtensorMap *out);
+cudaError_t tc_encode_w_tile(const ConvProblem &p, int block_k, int rows, CUtensorMap *out);
+cudaError_t tc_encode_y_rows(const ConvProblem &p, const void *base, int box_c, int box_m, CUtensorMap *out);
 // Dynamic shared memory of the tcgen05 kernel; `pair`: a 2-CTA pair holds half of each weight tile per CTA.
 int tc_smem_bytes(int block_n, int block_k, int stages, int pair);
 
@@ -148,6 +177,12 @@ cudaError_t fold_launch(const float *gamma, const float *beta, const float *mean
 // Thin-input tensor-core kernel (tc_gather.cu): 3x3 filters over 1, 3 or 4
 // channels, at most 64 output channels.
 bool gather_supported(const ConvProblem &p);
+struct GatherPlan {
+    int grid, tiles, block_n, block_k, stages, smem_bytes;
+    int pass_rows;  // output rows per staging pass at most (a CTA's whole share when its rows fit at once)
+};
+// The thin-input kernel's launch for this shape on `sm_count` SMs; false when it cannot run it.
+bool gather_plan(const ConvProblem &p, int sm_count, GatherPlan *out);
 cudaError_t gather_launch(const ConvProblem &p, int sm_count, cudaStream_t stream);
 cudaError_t gather_read_and_clear_error(cudaStream_t stream, unsigned int *out);
 constexpr int kGatherBlockThreads = 288;

@@ -90,23 +90,27 @@ struct WorkIter {
     // sequence, channel tile major.
     int g, g1;
     // vb / vg: this worker's index and the worker count (a CTA, or a CTA pair).
+    // The host enables balanced runs and stream-K only when the sequence length times
+    // the worker count fits in 32 bits, so the splits below use 32-bit divisions
+    // (64-bit ones would delay every CTA's first load by hundreds of cycles).
     __device__ WorkIter(const TcArgs &a, int vb, int vg)
     {
         state = 0;
         t = vb;
         stride = vg;
         if (a.balanced) {
-            const long long total = (long long)a.n_tiles * a.chunks_m;
-            g = (int)(total * vb / vg);
-            g1 = (int)(total * (vb + 1) / vg);
+            const uint32_t total = (uint32_t)a.n_tiles * (uint32_t)a.chunks_m;
+            g = (int)(total * (uint32_t)vb / (uint32_t)vg);
+            g1 = (int)(total * (uint32_t)(vb + 1) / (uint32_t)vg);
         }
         if (a.stream_k) {
-            const long long total = (long long)a.tiles * a.k_iters;
-            const long long g0 = total * vb / vg, g1 = total * (vb + 1) / vg;
-            const int t0 = (int)(g0 / a.k_iters);
-            const int kb0 = (int)(g0 - (long long)t0 * a.k_iters);
-            const int t1 = (int)((g1 - 1) / a.k_iters);
-            const int ke1 = (int)(g1 - (long long)t1 * a.k_iters);
+            const uint32_t total = (uint32_t)a.tiles * (uint32_t)a.k_iters;
+            const uint32_t g0 = total * (uint32_t)vb / (uint32_t)vg, g1 = total * (uint32_t)(vb + 1) / (uint32_t)vg;
+            const uint32_t ki = (uint32_t)a.k_iters;
+            const int t0 = (int)(g0 / ki);
+            const int kb0 = (int)(g0 - (uint32_t)t0 * ki);
+            const int t1 = (int)((g1 - 1) / ki);
+            const int ke1 = (int)(g1 - (uint32_t)t1 * ki);
             t_tail = kb0 > 0 ? t0 : -1;
             kb_tail = kb0;
             t_head = ke1 < a.k_iters ? t1 : -1;
@@ -271,6 +275,11 @@ constexpr int kEpiKindFp8 = 3;  // the launch's EpiMode with an fp8 e4m3 output 
 __device__ __forceinline__ void prefetch_l2(const void *p)
 {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ void prefetch_l1(const void *p)
+{
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 // Calls f(std::integral_constant<int, mode>) with the epilogue mode as a compile-time
@@ -623,6 +632,77 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (; wi.next(a, u); ++lt) {
             const int buf = lt & 1;
             const uint32_t tparity = (uint32_t)(lt >> 1) & 1u;
+            // Stream-K, pixel-major tiles: the two pieces of a split tile (the head of one
+            // worker's range and the tail of the next one's) meet in the slot of that worker
+            // boundary; a pair keeps one partial tile per M half.  Each worker runs its tail
+            // piece first, so the tail piece publishes its fp32 partial sums and the head
+            // piece, which its worker runs later, adds them and finishes the tile.  A sum of
+            // two fp32 values does not depend on their order: the result is deterministic.
+            const bool split = !SWAP && a.stream_k && (u.kb > 0 || u.ke < a.k_iters);
+            const bool publish = split && u.kb > 0;
+            const bool combine = split && u.kb == 0;
+            const int slot = (u.kb > 0 ? vb - 1 : vb) * (PAIR ? 2 : 1) + rank;
+            float4 *part = a.stream_k ? reinterpret_cast<float4 *>(a.partial) + (size_t)slot * (32 * BN)
+                                      : nullptr;
+            // When the combining piece is this worker's last unit, the other accumulator
+            // buffer stays idle during its K loop: the partner's partial sums are loaded
+            // into it then, so that the final epilogue reads them from tensor memory.
+            bool prefetched = false;
+            if (combine) {
+                WorkIter peek = wi;
+                WorkUnit q;
+                if (!peek.next(a, q)) {
+                    int got = 1;
+                    if (lane == 0)
+                        got = wait_flag_bounded(a.flags + slot * kTcFlagsPerSlot + ep, abort_flag, a.wait_ns) ? 1 : 0;
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!got) {
+                        if (lane == 0 && !*abort_flag) record_error(kErrTimeoutEpilogue, abort_flag);
+                        break;
+                    }
+                    __threadfence();
+                    const uint32_t t_other =
+                        tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)((buf ^ 1) * BN + col_base);
+#pragma unroll 1
+                    for (int c0 = 0; c0 < C::EPI_COLS; c0 += 64) {
+                        uint32_t pv[64];
+#pragma unroll
+                        for (int g = 0; g < 16; ++g) {
+                            const float4 p4 = __ldcg(part + (size_t)((col_base + c0) / 4 + g) * C::BM + row);
+                            pv[4 * g] = __float_as_uint(p4.x);
+                            pv[4 * g + 1] = __float_as_uint(p4.y);
+                            pv[4 * g + 2] = __float_as_uint(p4.z);
+                            pv[4 * g + 3] = __float_as_uint(p4.w);
+                        }
+#pragma unroll
+                        for (int q16 = 0; q16 < 4; ++q16)
+                            dev::tmem_st_32x32b_x16(t_other + (uint32_t)(c0 + 16 * q16), pv + 16 * q16);
+                    }
+                    dev::tmem_st_wait();
+                    __syncwarp();  // every lane has read the partial: the slot is free again
+                    if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 0);
+                    prefetched = true;
+                }
+            }
+            // The unit's per-channel scale and bias, read while its K loop still runs: the
+            // first touch of these lines otherwise costs an L2 round trip inside the epilogue.
+            float swap_hs = 0.f, swap_hb = 0.f;  // channel-major tiles: this thread's channel
+            if constexpr (SWAP) {
+                const int nt = a.balanced ? u.tile : u.tile - (u.tile / a.n_tiles) * a.n_tiles;
+                const int ch = nt * C::BM + ew * 32 + lane;
+                swap_hs = ch < a.c_out ? 0.5f * __ldg(a.scale + ch) : 0.f;
+                swap_hb = ch < a.c_out ? 0.5f * __ldg(a.bias + ch) : 0.f;
+            } else {
+                // One prefetch per 16 channels (64 bytes) of each array, so that every 128-byte
+                // line the warp's columns touch is covered whatever the arrays' alignment.
+                const int c0 = (u.tile - (u.tile / a.n_tiles) * a.n_tiles) * BN + col_base;
+                constexpr int NP = (C::EPI_COLS + 15) / 16;
+                static_assert(2 * NP <= 32, "one lane per prefetch");
+                if (lane < 2 * NP) {
+                    const int c = c0 + (lane % NP) * 16;
+                    if (c < a.c_out) prefetch_l1(lane < NP ? a.scale + c : a.bias + c);
+                }
+            }
             int ok = 1;
             if (lane == 0)
                 ok = dev::mbar_wait_bounded(dev::smem_u32(&tfull[buf]), tparity, abort_flag,
@@ -648,9 +728,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 int nt, p0, nchunks;
                 swap_geometry(u, nt, p0, nchunks);
                 const int ch_w0 = nt * C::BM + ew * 32;  // warp's first channel
-                const int ch = ch_w0 + lane;
-                const float hs = ch < a.c_out ? 0.5f * __ldg(a.scale + ch) : 0.f;
-                const float hb = ch < a.c_out ? 0.5f * __ldg(a.bias + ch) : 0.f;
+                const float hs = swap_hs, hb = swap_hb;
                 const uint32_t t_lane = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN);
                 if (half >= nchunks) {
                     // A unit narrower than two chunks leaves this warp nothing to read.
@@ -676,16 +754,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     if (lane == 0) dev::bulk_wait_group_read<1>();
                     __syncwarp();
-                    __nv_bfloat16 *sb = reinterpret_cast<__nv_bfloat16 *>(my_stg + sbuf * C::STG_BYTES);
-                    uint8_t *sb8 = my_stg + sbuf * C::STG_BYTES;  // fp8: rows of 32 one-byte channels
+                    // Staging rows: row pp holds pixel pp's 32 channels (2 bytes each, or 1 for fp8).
+                    const uint32_t sb = dev::smem_u32(my_stg + sbuf * C::STG_BYTES);
                     const int px0 = p0 + j * EC;
                     with_epi_mode<EPI>(emode, [&](auto mode_c) {
                         constexpr int md = decltype(mode_c)::value;
                         if constexpr (FP8) {
 #pragma unroll
                             for (int pp = 0; pp < EC; ++pp)  // row pp: 32 channels, one byte per lane
-                                sb8[pp * 32 + lane] =
-                                    dev::to_e4m3(dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, md));
+                                dev::sts_u8(sb + (uint32_t)(pp * 32 + lane),
+                                            dev::to_e4m3(dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, md)));
                         } else if constexpr (RES) {
                             // The residual tile is in the staging buffer (row pp: the pixel's 32
                             // channels); each lane adds its channel's column in place.
@@ -695,20 +773,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 f[pp] = dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, md);
                             residual_wait();
 #pragma unroll
-                            for (int pp = 0; pp < EC; ++pp)
-                                sb[pp * 32 + lane] =
-                                    __float2bfloat16_rn(f[pp] + __bfloat162float(sb[pp * 32 + lane]));
+                            for (int pp = 0; pp < EC; ++pp) {
+                                const uint32_t at = sb + (uint32_t)((pp * 32 + lane) * 2);
+                                dev::sts_u16(at, __bfloat16_as_ushort(__float2bfloat16_rn(
+                                                     f[pp] + dev::bf16_bits_to_float(dev::lds_u16(at)))));
+                            }
                         } else {
 #pragma unroll
                             for (int pp = 0; pp < EC; ++pp)  // row pp: 32 channels, one per lane
-                                sb[pp * 32 + lane] = __float2bfloat16_rn(
-                                    dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, md));
+                                dev::sts_u16(sb + (uint32_t)((pp * 32 + lane) * 2),
+                                             __bfloat16_as_ushort(__float2bfloat16_rn(
+                                                 dev::epilogue_from_half(__uint_as_float(v[pp]), hs, hb, md))));
                         }
                     });
                     dev::fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0 && px0 < a.m && ch_w0 < a.c_out) {
-                        dev::tma_store_2d(&tm_y, dev::smem_u32(sb), ch_w0, px0);
+                        dev::tma_store_2d(&tm_y, sb, ch_w0, px0);
                         dev::bulk_commit_group();
                     }
                     sbuf ^= 1;
@@ -719,26 +800,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int m_tile = PAIR ? 2 * m_unit + rank : m_unit;
             const int n0 = (u.tile - m_unit * a.n_tiles) * BN;
             const int row0 = m_tile * C::BM + ew * 32;  // first output pixel of this warp
-            // Stream-K: the two pieces of a split tile (the head of one worker's range
-            // and the tail of the next one's) meet in the slot of that worker boundary;
-            // a pair keeps one partial tile per M half.  Whichever piece's accumulator
-            // is ready first leaves its fp32 partial sums there; the other adds them
-            // and finishes the tile, so neither waits for the other to be computed.
-            // A sum of two fp32 values does not depend on their order: the result is
-            // the same whichever piece arrives first.
-            const bool split = a.stream_k && (u.kb > 0 || u.ke < a.k_iters);
-            const int slot = (u.kb > 0 ? vb - 1 : vb) * (PAIR ? 2 : 1) + rank;
-            bool publish = false, combine = false;
-            if (split) {
-                int first = 0;
-                if (lane == 0) first = atomicAdd(a.flags + slot * kTcFlagsPerSlot + kTcTicketOffset + ep, 1) == 0;
-                first = __shfl_sync(0xffffffffu, first, 0);
-                publish = first != 0;
-                combine = first == 0;
-            }
-            float4 *part = a.stream_k ? reinterpret_cast<float4 *>(a.partial) + (size_t)slot * (32 * BN)
-                                      : nullptr;
-            if (combine) {
+            if (combine && !prefetched) {
                 int got = 1;
                 if (lane == 0)
                     got = wait_flag_bounded(a.flags + slot * kTcFlagsPerSlot + ep, abort_flag, a.wait_ns) ? 1 : 0;
@@ -759,9 +821,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int q = 0; q < EC / 16; ++q)
                     dev::tmem_ld_32x32b_x16(t_lane + (uint32_t)(j * EC + q * 16), v + q * 16);
-                dev::tmem_ld_wait();
+                if (prefetched) {
+                    // The partner's partial sums, prefetched into the other accumulator buffer.
+                    uint32_t pv[EC];
+                    const uint32_t t_other = t_lane + (uint32_t)((buf ^ 1) * BN - buf * BN);
 #pragma unroll
-                for (int q = 0; q < EC / 16; ++q) dev::reg_fence16(v + q * 16);
+                    for (int q = 0; q < EC / 16; ++q)
+                        dev::tmem_ld_32x32b_x16(t_other + (uint32_t)(j * EC + q * 16), pv + q * 16);
+                    dev::tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < EC / 16; ++q) {
+                        dev::reg_fence16(v + q * 16);
+                        dev::reg_fence16(pv + q * 16);
+                    }
+#pragma unroll
+                    for (int i = 0; i < EC; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(pv[i]));
+                } else {
+                    dev::tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < EC / 16; ++q) dev::reg_fence16(v + q * 16);
+                }
                 if (j == C::EPI_COLS / EC - 1) {
                     // The accumulator is in registers: hand the TMEM buffer back to the MMA warp.
                     dev::tc_fence_before_sync();
@@ -782,7 +861,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
                     continue;
                 }
-                if (combine) {
+                if (combine && !prefetched) {
 #pragma unroll
                     for (int q = 0; q < EC / 4; ++q) {
                         const float4 p4 = __ldcg(part + (size_t)((col_base + j * EC) / 4 + q) * C::BM + row);
@@ -837,11 +916,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             }
                         }
                         residual_wait();
-                        const uint8_t *rb = my_stg + sbuf * C::STG_BYTES;
+                        const uint32_t rb = dev::smem_u32(my_stg + sbuf * C::STG_BYTES);
 #pragma unroll
                         for (int q = 0; q < ROW_Y / 16; ++q) {
-                            const uint4 r4 = *reinterpret_cast<const uint4 *>(
-                                rb + swizzle_offset<ROW_Y>((uint32_t)(lane * ROW_Y + q * 16)));
+                            const uint4 r4 = dev::lds_v4(rb + swizzle_offset<ROW_Y>((uint32_t)(lane * ROW_Y + q * 16)));
                             const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
@@ -878,28 +956,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // Stage the warp's 32 rows x EC channels, then one TMA store.
                 if (lane == 0) dev::bulk_wait_group_read<1>();
                 __syncwarp();
-                uint8_t *sb = my_stg + sbuf * C::STG_BYTES;
+                const uint32_t sb = dev::smem_u32(my_stg + sbuf * C::STG_BYTES);
                 if constexpr (FP8) {
                     // One byte per value: rows of EC bytes (32: 32-byte swizzle; 16: none).
 #pragma unroll
                     for (int q = 0; q < EC / 16; ++q) {
                         const uint32_t raw = (uint32_t)(lane * EC + q * 16);
                         const uint32_t off = EC == 32 ? swizzle_offset<32>(raw) : raw;
-                        *reinterpret_cast<uint4 *>(sb + off) = make_uint4(q8[4 * q], q8[4 * q + 1], q8[4 * q + 2],
-                                                                          q8[4 * q + 3]);
+                        dev::sts_v4(sb + off, q8[4 * q], q8[4 * q + 1], q8[4 * q + 2], q8[4 * q + 3]);
                     }
                 } else {
 #pragma unroll
-                for (int q = 0; q < ROW_Y / 16; ++q) {
-                    const uint32_t off = swizzle_offset<ROW_Y>((uint32_t)(lane * ROW_Y + q * 16));
-                    *reinterpret_cast<uint4 *>(sb + off) =
-                        make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-                }
+                    for (int q = 0; q < ROW_Y / 16; ++q) {
+                        const uint32_t off = swizzle_offset<ROW_Y>((uint32_t)(lane * ROW_Y + q * 16));
+                        dev::sts_v4(sb + off, packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                    }
                 }
                 dev::fence_proxy_async_shared();
                 __syncwarp();
                 if (lane == 0 && row0 < a.m && ch0 < a.c_out) {
-                    dev::tma_store_2d(&tm_y, dev::smem_u32(sb), ch0, row0);
+                    dev::tma_store_2d(&tm_y, sb, ch0, row0);
                     dev::bulk_commit_group();
                 }
                 sbuf ^= 1;
@@ -909,12 +985,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 1);
-            } else if (combine) {
+            } else if (combine && !prefetched) {
                 __syncwarp();  // all lanes have read the partial: the slot is free again
-                if (lane == 0) {
-                    st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 0);
-                    a.flags[slot * kTcFlagsPerSlot + kTcTicketOffset + ep] = 0;
-                }
+                if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 0);
             }
         }
         if constexpr (RES) {
@@ -998,44 +1071,102 @@ static cudaError_t encode_bf16_like_y(const ConvProblem &p, int block_n, bool sw
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swap, bool pair, TcMaps *maps)
+}  // namespace
+
+cudaError_t tc_encode_x_im2col(const ConvProblem &p, int block_k, int box_pixels, CUtensorMap *out)
 {
     cudaError_t st = load_encoders();
     if (st != cudaSuccess) return st;
-    const CUtensorMapSwizzle sw_k = swizzle_for_row_bytes(block_k * 2);
     // x: im2col view over (C, W, H, N).  The bounding box of window corners is
     // [-pad, dim - 1 + pad - (filter - 1)] along W and H, traversed with the
-    // convolution stride, so a box of 128 pixels walks output pixels in
+    // convolution stride, so a box of `box_pixels` pixels walks output pixels in
     // (img, oh, ow) order, crossing rows and images.
-    {
-        cuuint64_t dims[4] = {(cuuint64_t)p.c, (cuuint64_t)p.w_in, (cuuint64_t)p.h, (cuuint64_t)p.n};
-        cuuint64_t strides[3] = {(cuuint64_t)p.c * 2, (cuuint64_t)p.w_in * p.c * 2,
-                                 (cuuint64_t)p.h * p.w_in * p.c * 2};
-        int lower[2] = {-p.pad_w, -p.pad_h};
-        int upper[2] = {p.pad_w - (p.s - 1), p.pad_h - (p.r - 1)};
-        cuuint32_t estr[4] = {1, (cuuint32_t)p.stride_w, (cuuint32_t)p.stride_h, 1};
-        CUresult r = g_encode_im2col(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(p.x),
-                                     dims, strides, lower, upper, (cuuint32_t)block_k,
-                                     (cuuint32_t)kTcBlockM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw_k,
-                                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
-    // W: (C, R*S, C_out), box (BK, 1, BN).
-    {
-        cuuint64_t dims[3] = {(cuuint64_t)p.c, (cuuint64_t)p.r * p.s, (cuuint64_t)p.c_out};
-        cuuint64_t strides[2] = {(cuuint64_t)p.c * 2, (cuuint64_t)p.r * p.s * p.c * 2};
-        // Rows of one load: the whole N tile, the 128-channel A tile when swapped,
-        // or half the N tile per CTA of a 2-CTA pair.
-        const int rows = swap ? kTcBlockM : (pair ? block_n / 2 : block_n);
-        cuuint32_t box[3] = {(cuuint32_t)block_k, 1, (cuuint32_t)rows};
-        cuuint32_t estr[3] = {1, 1, 1};
-        CUresult r = g_encode_tiled(&maps->w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.w),
-                                    dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw_k,
-                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
+    cuuint64_t dims[4] = {(cuuint64_t)p.c, (cuuint64_t)p.w_in, (cuuint64_t)p.h, (cuuint64_t)p.n};
+    cuuint64_t strides[3] = {(cuuint64_t)p.c * 2, (cuuint64_t)p.w_in * p.c * 2, (cuuint64_t)p.h * p.w_in * p.c * 2};
+    int lower[2] = {-p.pad_w, -p.pad_h};
+    int upper[2] = {p.pad_w - (p.s - 1), p.pad_h - (p.r - 1)};
+    cuuint32_t estr[4] = {1, (cuuint32_t)p.stride_w, (cuuint32_t)p.stride_h, 1};
+    CUresult r = g_encode_im2col(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(p.x), dims, strides,
+                                 lower, upper, (cuuint32_t)block_k, (cuuint32_t)box_pixels, estr,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for_row_bytes(block_k * 2),
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t tc_encode_x_rows(const ConvProblem &p, int block_k, int rows, CUtensorMap *out)
+{
+    cudaError_t st = load_encoders();
+    if (st != cudaSuccess) return st;
+    // x viewed as (stride*C, W/stride, H, N): input pixel stride*j + e is element e of view
+    // pixel j.  Box: block_k channels of wo view pixels over `rows` input rows taken every
+    // stride-th row (the rows one filter tap of `rows` output rows reads).
+    const int sd = p.stride_w;
+    cuuint64_t dims[4] = {(cuuint64_t)sd * p.c, (cuuint64_t)(p.w_in / sd), (cuuint64_t)p.h, (cuuint64_t)p.n};
+    cuuint64_t strides[3] = {(cuuint64_t)sd * p.c * 2, (cuuint64_t)p.w_in * p.c * 2, (cuuint64_t)p.h * p.w_in * p.c * 2};
+    cuuint32_t box[4] = {(cuuint32_t)block_k, (cuuint32_t)p.wo, (cuuint32_t)(p.stride_h * (rows - 1) + 1), 1};
+    cuuint32_t estr[4] = {1, 1, (cuuint32_t)p.stride_h, 1};
+    CUresult r = g_encode_tiled(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(p.x), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for_row_bytes(block_k * 2),
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t tc_encode_x_matrix(const ConvProblem &p, int block_k, int box_rows, CUtensorMap *out)
+{
+    cudaError_t st = load_encoders();
+    if (st != cudaSuccess) return st;
+    cuuint64_t dims[2] = {(cuuint64_t)p.c, (cuuint64_t)p.m};
+    cuuint64_t strides[1] = {(cuuint64_t)p.c * 2};
+    cuuint32_t box[2] = {(cuuint32_t)block_k, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode_tiled(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(p.x), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for_row_bytes(block_k * 2),
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t tc_encode_w_tile(const ConvProblem &p, int block_k, int rows, CUtensorMap *out)
+{
+    cudaError_t st = load_encoders();
+    if (st != cudaSuccess) return st;
+    // W: (C, R*S, C_out), box (BK, 1, rows): one filter tap's BK channels of `rows` output channels.
+    cuuint64_t dims[3] = {(cuuint64_t)p.c, (cuuint64_t)p.r * p.s, (cuuint64_t)p.c_out};
+    cuuint64_t strides[2] = {(cuuint64_t)p.c * 2, (cuuint64_t)p.r * p.s * p.c * 2};
+    cuuint32_t box[3] = {(cuuint32_t)block_k, 1, (cuuint32_t)rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode_tiled(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.w), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for_row_bytes(block_k * 2),
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t tc_encode_y_rows(const ConvProblem &p, const void *base, int box_c, int box_m, CUtensorMap *out)
+{
+    cudaError_t st = load_encoders();
+    if (st != cudaSuccess) return st;
+    // A tensor shaped like y, viewed as (C_out, M), unswizzled box (box_c, box_m); bf16, or
+    // one byte per element for the fp8 output.
+    cuuint64_t dims[2] = {(cuuint64_t)p.c_out, (cuuint64_t)p.m};
+    cuuint64_t strides[1] = {(cuuint64_t)p.c_out * (p.out_fp8 ? 1 : 2)};
+    cuuint32_t box[2] = {(cuuint32_t)box_c, (cuuint32_t)box_m};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode_tiled(out, p.out_fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+namespace {
+
+cudaError_t encode_maps(const ConvProblem &p, int block_n, int block_k, bool swap, bool pair, TcMaps *maps)
+{
+    cudaError_t st = tc_encode_x_im2col(p, block_k, kTcBlockM, &maps->x);
+    if (st != cudaSuccess) return st;
+    // W rows of one load: the whole N tile, the 128-channel A tile when swapped, or half
+    // the N tile per CTA of a 2-CTA pair.
+    st = tc_encode_w_tile(p, block_k, swap ? kTcBlockM : (pair ? block_n / 2 : block_n), &maps->w);
+    if (st != cudaSuccess) return st;
     // y: (C_out, M), box (EC, 32): one epilogue warp's rows, one column chunk.
     if (p.out_fp8) {
         // fp8 e4m3 output, one byte per element: rows of EC bytes (pixel-major), or for
@@ -1324,7 +1455,7 @@ static long long swap_boxes_balanced(long long m, int n_tiles, int grid)
 
 int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *rq, TcPlan *out)
 {
-    const PlanRequest dflt{-1, -1, -1, 0, -1};
+    const PlanRequest dflt{-1, -1, -1, 0, -1, -1, -1};
     const PlanRequest &q = rq ? *rq : dflt;
     if (q.block_n != 0 && !valid_block_n(q.block_n)) return -1;
     TcPlan t{};
@@ -1375,6 +1506,26 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
                     ? 1
                     : 0;
     if (q.swap_ab >= 0) t.swap_ab = q.swap_ab ? 1 : 0;
+    // Channel-major tiles on the kernel of tc_cmajor.cu: x in boxes of whole output rows
+    // where the shape allows (the planner's choice), or im2col boxes; the weights streamed
+    // with every K step, or resident in tensor memory on request.
+    const bool want_cm = q.wres == 1 || q.row_boxes == 1 || (q.wres < 0 && q.row_boxes < 0 && t.swap_ab);
+    if (want_cm) {
+        const bool overrides = q.block_n != 0 || q.stream_k == 1 || q.pair == 1 || q.balanced >= 0 || q.swap_ab == 0;
+        TcPlan w{};
+        if (!overrides) {
+            const int wres = q.wres == 1 ? 1 : 0;
+            if (q.row_boxes != 0 && cmajor_fill_plan(p, sm_count, wres, 1, &w)) {
+                *out = w;
+                return 0;
+            }
+            if (q.row_boxes != 1 && (q.wres == 1 || q.row_boxes == 0) && cmajor_fill_plan(p, sm_count, wres, 0, &w)) {
+                *out = w;
+                return 0;
+            }
+        }
+        if (q.wres == 1 || q.row_boxes == 1) return -1;
+    }
     if (t.swap_ab) {
         // The channel-major tile is 128 channels x up to 256 pixels.  Whole 256-pixel
         // tiles leave a partly idle last wave (the pointwise layer: 200 tiles on 152
@@ -1394,9 +1545,12 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
         const long long chunks = (p.m + 31) / 32 * t.n_tiles;
         const int grid_bal = (int)std::min<long long>(chunks, sm_count);
         const int grid_whole = std::min(t.tiles, sm_count);
+        // The kernel splits the chunk sequence with 32-bit arithmetic.
+        const bool bal_fits = chunks * grid_bal < (1LL << 32);
+        if (q.balanced == 1 && !bal_fits) return -1;
         t.balanced = q.balanced >= 0 ? q.balanced
-                                     : (swap_small || 4 * swap_boxes_balanced(p.m, t.n_tiles, grid_bal) <=
-                                                          3 * swap_boxes_whole(t.tiles, grid_whole)
+                                     : (bal_fits && (swap_small || 4 * swap_boxes_balanced(p.m, t.n_tiles, grid_bal) <=
+                                                                       3 * swap_boxes_whole(t.tiles, grid_whole))
                                             ? 1
                                             : 0);
         t.grid = t.balanced ? grid_bal : grid_whole;
@@ -1421,7 +1575,9 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
     // takes total/grid consecutive K steps.  Each share must cover at least one
     // tile so that a tile is split between two CTAs at most.
     const long long total = (long long)t.tiles * t.k_iters;
-    const bool sk_possible = total / sm_count >= t.k_iters;
+    // Each share covers at least one tile; the kernel splits the K-step sequence with
+    // 32-bit arithmetic.
+    const bool sk_possible = total / sm_count >= t.k_iters && total * sm_count < (1LL << 32);
     t.stream_k = (t.tiles > sm_count && t.tiles % sm_count != 0 && t.tiles < 4LL * sm_count &&
                   t.k_iters >= 16 && sk_possible)
                      ? 1
@@ -1520,6 +1676,7 @@ cudaError_t dispatch(const ConvProblem &p, const TcPlan &plan, const TcMaps &map
 cudaError_t tc_launch_with_workspace(const ConvProblem &p, const TcPlan &plan, cudaStream_t stream,
                                      void *workspace)
 {
+    if (plan.cmajor) return cmajor_launch(p, plan, stream);
     TcMaps maps;
     cudaError_t st = cached_maps(p, plan.block_n, plan.block_k, plan.swap_ab != 0, plan.pair != 0, &maps);
     if (st != cudaSuccess) return st;

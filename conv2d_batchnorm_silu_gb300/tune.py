@@ -57,6 +57,11 @@ def variants():
     """(label, overrides) for every alternative; unsupported ones are skipped per shape."""
     yield "auto", {}
     yield "direct", {"algo": "direct"}
+    # channel-major tiles on the kernel of tc_cmajor.cu: x in boxes of whole output rows (or of
+    # the [M][C] matrix of a 1x1 layer) or in im2col boxes, the weights streamed or resident
+    yield "rows", {"algo": "tcgen05", "row_boxes": 1, "weights_resident": 0}
+    yield "rows-wres", {"algo": "tcgen05", "row_boxes": 1, "weights_resident": 1}
+    yield "wres", {"algo": "tcgen05", "row_boxes": 0, "weights_resident": 1}
     for swap, sk, pair, bn in itertools.product((0, 1), (0, 1), (0, 1), (128, 256)):
         if swap and (sk or pair or bn != 256):
             continue
@@ -64,9 +69,10 @@ def variants():
             continue
         if swap:
             # channel-major: equal runs of 32-pixel chunks, or whole 256-pixel tiles
-            yield "swap", {"algo": "tcgen05", "swap_ab": 1, "stream_k": 0, "pair": 0, "block_n": 0, "balanced": 1}
+            yield "swap", {"algo": "tcgen05", "swap_ab": 1, "stream_k": 0, "pair": 0, "block_n": 0, "balanced": 1,
+                           "weights_resident": 0, "row_boxes": 0}
             yield "swap-tiles", {"algo": "tcgen05", "swap_ab": 1, "stream_k": 0, "pair": 0, "block_n": 0,
-                                 "balanced": 0}
+                                 "balanced": 0, "weights_resident": 0, "row_boxes": 0}
             continue
         label = f"n{bn}{'-sk' if sk else ''}{'-pair' if pair else ''}"
         yield label, {"algo": "tcgen05", "swap_ab": swap, "stream_k": sk, "pair": pair, "block_n": bn}
@@ -141,6 +147,10 @@ def _plan_label(pl: dict) -> str:
         return "direct"
     if pl["threads"] != 384:
         return "thin-input"
+    if pl.get("row_boxes"):
+        return "rows-wres" if pl.get("weights_resident") else "rows"
+    if pl.get("weights_resident"):
+        return "wres"
     if pl["swap_ab"]:
         return "swap" if pl.get("balanced") else "swap-tiles"
     return f"n{pl['block_n']}{'-sk' if pl['stream_k'] else ''}{'-pair' if pl['cluster'] == 2 else ''}"

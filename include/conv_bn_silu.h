@@ -262,6 +262,10 @@ typedef struct cbs_plan_info {
     long long workspace_bytes; /* library-held scratch for stream-K partial tiles (0 if none) */
     int balanced;     /* swap_ab only: 1 when each CTA takes an equal run of 32-pixel chunks (units of at
                          most 256 pixels) instead of whole 256-pixel tiles */
+    int weights_resident; /* swap_ab only: 1 when each CTA keeps its 128-channel weight tile in tensor
+                             memory for the whole kernel and streams only x (units of block_m pixels) */
+    int row_boxes;    /* swap_ab only: 1 when x is loaded in boxes of whole output rows (units of
+                         block_m pixels = whole rows of one image) instead of im2col boxes */
 } cbs_plan_info;
 
 /* Fills `info` for the given shape, algorithm and SM count (sm_count > 0;
@@ -291,6 +295,12 @@ typedef struct cbs_plan_request {
                                   test.)  Ignored by the other kernels. */
     int balanced; /* -1, or (channel-major tiles only) 0: whole 256-pixel tiles dealt round-robin,
                      1: each CTA an equal run of 32-pixel chunks */
+    int weights_resident; /* -1, or 0: weights loaded with every tile, 1: the weight tile resident in
+                             tensor memory (channel-major tiles, bf16 output without a residual, when
+                             the tile fits next to two accumulators) */
+    int row_boxes;        /* -1, or (channel-major tiles, bf16 output without a residual) 1: x loaded in
+                             boxes of whole output rows (W divisible by the stride, equal strides, up
+                             to 256 output columns), 0: im2col boxes */
 } cbs_plan_request;
 
 /* conv_bn_silu_plan with overrides.  CBS_ERR_INVALID_ARG for an out-of-range

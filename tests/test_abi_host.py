@@ -72,9 +72,17 @@ def test_plan_for_the_five_layers(lib):
             assert p["block_m"] == 128 and p["block_n"] == 16 and p["block_k"] == 32
             assert p["tiles"] == 800 and p["grid"] == 304 and p["smem_bytes"] <= 113 * 1024
             continue
+        if name in ("down", "pointwise"):
+            # channel-major tiles, x in boxes of whole output rows (the 1x1 layer: of its
+            # [M][C] matrix), weights loaded with every K step; units of block_m pixels
+            assert p["swap_ab"] == 1 and p["row_boxes"] == 1 and p["weights_resident"] == 0, p
+            assert p["block_m"] % 16 == 0 and p["block_m"] <= 256 and p["block_n"] == 128
+            assert p["grid"] == 152 and p["stream_k"] == 0 and p["cluster"] == 1
+            assert p["smem_bytes"] <= 232448 and p["stages"] >= 3
+            continue
         if p["algo"] == "tcgen05":
-            assert p["swap_ab"] == (1 if name in ("down", "pointwise") else 0)
-            assert p["block_m"] == (256 if p["swap_ab"] else 128)
+            assert p["swap_ab"] == 0
+            assert p["block_m"] == 128
             assert p["block_n"] % 16 == 0 and p["block_n"] <= 256
             assert p["block_n"] >= min(sh.k, 128)
             assert p["stream_k"] == (1 if name == "deep" else 0)
@@ -233,13 +241,13 @@ def test_balanced_channel_major_plans(lib):
     """Channel-major (swap AB) plans deal equal runs of 32-pixel chunks by default; whole
     256-pixel tiles on request; a balanced run is refused on pixel-major tiles."""
     pointwise = (16, 40, 40, 256, 256, 1, 1, 1, 0)   # 200 whole tiles: 48 CTAs would take two
-    p = lib.plan_request(*pointwise)
-    assert p["swap_ab"] == 1 and p["balanced"] == 1 and p["grid"] == 152
+    p = lib.plan_request(*pointwise, row_boxes=0)      # the tc_conv.cu channel-major kernel
+    assert p["swap_ab"] == 1 and p["balanced"] == 1 and p["grid"] == 152 and p["row_boxes"] == 0
     p0 = lib.plan_request(*pointwise, balanced=0)
     assert p0["swap_ab"] == 1 and p0["balanced"] == 0 and p0["grid"] == 152 and p0["tiles"] == 200
-    assert lib.plan(*pointwise)["balanced"] == 1
+    assert lib.plan(*pointwise)["row_boxes"] == 1
     tiny_swap = (2, 13, 11, 16, 24, 3, 3, 1, 1)      # 286 pixels: 9 chunks, so 9 CTAs
-    assert lib.plan_request(*tiny_swap, swap_ab=1)["grid"] == 9
+    assert lib.plan_request(*tiny_swap, swap_ab=1, row_boxes=0)["grid"] == 9
     assert lib.plan_request(*tiny_swap, swap_ab=1, balanced=0)["grid"] == 2
     deep = (32, 20, 20, 512, 512, 3, 3, 1, 1)
     assert lib.plan_request(*deep)["balanced"] == 0
@@ -255,6 +263,10 @@ def test_tuning_sweep_variants_are_consistent():
     labels = [v[0] for v in vs]
     assert len(labels) == len(set(labels)) and labels[:2] == ["auto", "direct"]
     for label, ov in vs[2:]:
+        if "row_boxes" in ov and "swap_ab" not in ov:   # the channel-major kernel of tc_cmajor.cu
+            assert ov["row_boxes"] in (0, 1) and ov["weights_resident"] in (0, 1)
+            assert ov["row_boxes"] or ov["weights_resident"]
+            continue
         assert not (ov["pair"] and not ov["stream_k"])
         assert not (ov["swap_ab"] and (ov["stream_k"] or ov["pair"]))
         assert ov.get("balanced", -1) != 1 or ov["swap_ab"] == 1
@@ -263,16 +275,17 @@ def test_tuning_sweep_variants_are_consistent():
 
 
 def test_planner_choices_match_the_measured_sweep():
-    """The planner's choice for every layer of the threshold sweep, as measured on a GB300
-    (152 SMs) and recorded with the sweep's timings: a change to the planner's rules changes
-    one of these and calls for the sweep to be run again."""
+    """The planner's choice for every layer of the threshold sweep (tune.SWEEP) on a
+    152-SM GB300, as the sweep recorded in profiles/planner_sweep_yolo_layers.md measured
+    it: a change to the planner's rules changes one of these and calls for the sweep to
+    be run again."""
     from conv2d_batchnorm_silu_gb300 import capi, tune
     expected = {
-        "stem640": "thin-input", "down320": "swap-tiles", "c2f160_1x1": "n64", "bneck160": "swap-tiles",
-        "down160": "swap", "c2f80_1x1": "swap", "bneck80": "swap", "down80": "swap-tiles",
-        "c2f40_1x1": "swap-tiles", "bneck40": "swap", "down40": "swap", "c2f20_1x1": "swap",
-        "bneck20": "n128", "sppf20_1x1": "n128", "head80_3x3": "swap", "tiny": "n32",
-        "stem": "thin-input", "down": "swap-tiles", "pointwise": "swap", "deep": "n256-sk-pair",
+        "stem640": "thin-input", "down320": "rows", "c2f160_1x1": "n64", "bneck160": "rows",
+        "down160": "rows", "c2f80_1x1": "rows", "bneck80": "rows", "down80": "rows",
+        "c2f40_1x1": "rows", "bneck40": "rows", "down40": "rows", "c2f20_1x1": "rows",
+        "bneck20": "n128", "sppf20_1x1": "n128", "head80_3x3": "rows", "tiny": "n32",
+        "stem": "thin-input", "down": "rows", "pointwise": "rows", "deep": "n256-sk-pair",
     }
     got = {}
     for sh in tune.SWEEP:
