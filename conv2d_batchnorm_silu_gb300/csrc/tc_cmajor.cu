@@ -433,11 +433,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             dev::tc_fence_after_sync();
             const int nchunks = (u.np + kCmChunk - 1) / kCmChunk;
             const uint32_t t_lane = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(wcols + buf * a.unit_px);
-            if (half >= nchunks) {
-                // A unit of one chunk leaves this warp nothing to read.
+            if (half >= nchunks || ch_w0 >= a.c_out) {
+                // A unit of one chunk, or a lane quarter past the last output channel, leaves
+                // this warp nothing to read or store.
                 dev::tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
+                continue;
             }
 #pragma unroll 1
             for (int j = half; j < nchunks; j += 2) {
@@ -476,7 +478,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 dev::fence_proxy_async_shared();
                 __syncwarp();
                 const int px0 = u.p0 + j * kCmChunk;
-                if (lane == 0 && ch_w0 < a.c_out) {
+                if (lane == 0) {
                     dev::tma_store_2d(&tm_y, sb, ch_w0, px0);  // TMA clips channels >= c_out and pixels >= m
                     dev::bulk_commit_group();
                 }
@@ -546,15 +548,18 @@ cudaError_t launch_cm(const ConvProblem &p, const TcPlan &plan, const CmMaps &ma
                              maps.x, maps.w, maps.y, a);
 }
 
-// Tensor maps of recent calls, keyed by pointers, shape and unit geometry.
+// Tensor maps of recent calls, keyed by pointers, shape, x mode and unit geometry.  The
+// x mode is part of the key: an im2col load issued with a tiled map (or the reverse) is
+// an illegal instruction, and two modes can share every other field (a 1x1 layer's
+// matrix-row units and its im2col units may have the same pixel count).
 struct CmKey {
     const void *x, *w, *y;
     int dims[11];
-    int unit_px, unit_rows, block_k, device;
+    int xmode, unit_px, unit_rows, block_k, device;
     bool operator==(const CmKey &o) const
     {
-        if (x != o.x || w != o.w || y != o.y || unit_px != o.unit_px || unit_rows != o.unit_rows ||
-            block_k != o.block_k || device != o.device)
+        if (x != o.x || w != o.w || y != o.y || xmode != o.xmode || unit_px != o.unit_px ||
+            unit_rows != o.unit_rows || block_k != o.block_k || device != o.device)
             return false;
         for (int i = 0; i < 11; ++i)
             if (dims[i] != o.dims[i]) return false;
@@ -581,6 +586,7 @@ cudaError_t cm_maps(const ConvProblem &p, const TcPlan &plan, CmMaps *out)
     k.y = p.y;
     const int d[11] = {p.n, p.h, p.w_in, p.c, p.c_out, p.r, p.s, p.stride_h, p.stride_w, p.pad_h, p.pad_w};
     for (int i = 0; i < 11; ++i) k.dims[i] = d[i];
+    k.xmode = plan.cm_xmode;
     k.unit_px = plan.cm_unit_px;
     k.unit_rows = plan.cm_unit_rows;
     k.block_k = plan.block_k;

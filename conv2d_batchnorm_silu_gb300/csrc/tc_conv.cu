@@ -663,11 +663,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     __threadfence();
                     const uint32_t t_other =
                         tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)((buf ^ 1) * BN + col_base);
+                    // At most 64 of the warp's columns per pass, never more than it owns.
+                    constexpr int PC = C::EPI_COLS < 64 ? C::EPI_COLS : 64;
+                    static_assert(PC % 16 == 0 && C::EPI_COLS % PC == 0, "whole 16-column stores");
 #pragma unroll 1
-                    for (int c0 = 0; c0 < C::EPI_COLS; c0 += 64) {
-                        uint32_t pv[64];
+                    for (int c0 = 0; c0 < C::EPI_COLS; c0 += PC) {
+                        uint32_t pv[PC];
 #pragma unroll
-                        for (int g = 0; g < 16; ++g) {
+                        for (int g = 0; g < PC / 4; ++g) {
                             const float4 p4 = __ldcg(part + (size_t)((col_base + c0) / 4 + g) * C::BM + row);
                             pv[4 * g] = __float_as_uint(p4.x);
                             pv[4 * g + 1] = __float_as_uint(p4.y);
@@ -675,7 +678,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             pv[4 * g + 3] = __float_as_uint(p4.w);
                         }
 #pragma unroll
-                        for (int q16 = 0; q16 < 4; ++q16)
+                        for (int q16 = 0; q16 < PC / 16; ++q16)
                             dev::tmem_st_32x32b_x16(t_other + (uint32_t)(c0 + 16 * q16), pv + 16 * q16);
                     }
                     dev::tmem_st_wait();
@@ -738,6 +741,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
 #pragma unroll 1
                 for (int j = half; j < nchunks; j += C::SPLIT) {
+                    // A chunk wholly past the last pixel or channel is skipped (no staging write
+                    // without its store: the wait before each write counts one store per chunk).
+                    if (p0 + j * EC >= a.m || ch_w0 >= a.c_out) {
+                        if (j + C::SPLIT >= nchunks) {
+                            dev::tc_fence_before_sync();
+                            __syncwarp();
+                            if (lane == 0) dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
+                        }
+                        continue;
+                    }
                     if constexpr (RES) residual_load(ch_w0, p0 + j * EC);
                     uint32_t v[EC];
 #pragma unroll
@@ -788,7 +801,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     });
                     dev::fence_proxy_async_shared();
                     __syncwarp();
-                    if (lane == 0 && px0 < a.m && ch_w0 < a.c_out) {
+                    if (lane == 0) {  // a live chunk: TMA clips the pixels past m
                         dev::tma_store_2d(&tm_y, sb, ch_w0, px0);
                         dev::bulk_commit_group();
                     }
@@ -815,6 +828,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN + col_base);
 #pragma unroll 1
             for (int j = 0; j < C::EPI_COLS / EC; ++j) {
+                // A chunk wholly past the last output channel or pixel is skipped: nothing of it
+                // is stored (nor published), and it must not touch a staging buffer either, since
+                // the wait before each staging write counts one store per staged chunk.
+                if (row0 >= a.m || n0 + col_base + j * EC >= a.c_out) {
+                    if (j == C::EPI_COLS / EC - 1) {
+                        dev::tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (PAIR && rank != 0)
+                                dev::mbar_arrive_cluster(tempty0 + (uint32_t)(buf * 8));
+                            else
+                                dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
+                        }
+                    }
+                    continue;
+                }
                 if constexpr (RES)
                     if (!publish) residual_load(n0 + col_base + j * EC, row0);
                 uint32_t v[EC];
@@ -974,7 +1003,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 dev::fence_proxy_async_shared();
                 __syncwarp();
-                if (lane == 0 && row0 < a.m && ch0 < a.c_out) {
+                if (lane == 0) {  // a live chunk: TMA clips the channels past c_out and rows past m
                     dev::tma_store_2d(&tm_y, sb, ch0, row0);
                     dev::bulk_commit_group();
                 }
@@ -1506,25 +1535,64 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
                     ? 1
                     : 0;
     if (q.swap_ab >= 0) t.swap_ab = q.swap_ab ? 1 : 0;
-    // Channel-major tiles on the kernel of tc_cmajor.cu: x in boxes of whole output rows
-    // where the shape allows (the planner's choice), or im2col boxes; the weights streamed
-    // with every K step, or resident in tensor memory on request.
-    const bool want_cm = q.wres == 1 || q.row_boxes == 1 || (q.wres < 0 && q.row_boxes < 0 && t.swap_ab);
-    if (want_cm) {
-        const bool overrides = q.block_n != 0 || q.stream_k == 1 || q.pair == 1 || q.balanced >= 0 || q.swap_ab == 0;
+    // Channel-major tiles on the kernel of tc_cmajor.cu: x in tiled boxes of whole output
+    // rows (or of the [M][C] matrix of a 1x1 layer) or in im2col boxes; the weights streamed
+    // with every K step or resident in tensor memory.
+    const bool overrides = q.block_n != 0 || q.stream_k == 1 || q.pair == 1 || q.balanced >= 0 || q.swap_ab == 0;
+    if (q.wres == 1 || q.row_boxes == 1) {
+        // Requested explicitly.
         TcPlan w{};
-        if (!overrides) {
-            const int wres = q.wres == 1 ? 1 : 0;
-            if (q.row_boxes != 0 && cmajor_fill_plan(p, sm_count, wres, 1, &w)) {
-                *out = w;
-                return 0;
-            }
-            if (q.row_boxes != 1 && (q.wres == 1 || q.row_boxes == 0) && cmajor_fill_plan(p, sm_count, wres, 0, &w)) {
+        if (overrides) return -1;
+        const int wres = q.wres == 1 ? 1 : 0;
+        if (q.row_boxes != 0 && cmajor_fill_plan(p, sm_count, wres, 1, &w)) {
+            *out = w;
+            return 0;
+        }
+        if (q.row_boxes != 1 && cmajor_fill_plan(p, sm_count, wres, 0, &w)) {
+            *out = w;
+            return 0;
+        }
+        return -1;
+    }
+    if (q.wres < 0 && q.row_boxes < 0 && !overrides) {
+        // The planner's own choice, from the measured sweep of YOLO-shaped layers (the package's
+        // tune module).  Tiled boxes move at about 1.5x the rate of im2col boxes but only pay
+        // with 64-channel K steps (128-byte box rows):
+        //  - 1x1 layers read x as a matrix: matrix-row units won or tied on every such layer;
+        //  - stride-2 layers: whole-row units won where they spread as evenly over the SMs as
+        //    the im2col runs (the busiest CTA's pixels no more than its im2col box pixels), and
+        //    lost by about 10% where they did not (row units come in whole rows only);
+        //  - 3x3 stride-1 layers: im2col runs won on every such layer.
+        // With 32-channel K steps on a 3x3 filter and a large layer, im2col units with the
+        // weights resident in tensor memory won by 6-28%: the weight tile is a third of each
+        // K step's bytes there, and the MMA (A from tensor memory) still has time to spare.
+        const bool matrix =
+            p.r == 1 && p.s == 1 && p.stride_h == 1 && p.stride_w == 1 && p.pad_h == 0 && p.pad_w == 0;
+        TcPlan w{};
+        if (t.block_k == 64 && matrix && cmajor_fill_plan(p, sm_count, 0, 1, &w)) {
+            *out = w;
+            return 0;
+        }
+        if (t.swap_ab && p.c <= 32 && p.r * p.s >= 9 && p.m >= 256LL * sm_count &&
+            cmajor_fill_plan(p, sm_count, 1, 0, &w)) {
+            *out = w;
+            return 0;
+        }
+        if (t.swap_ab && t.block_k == 64 && (p.stride_h > 1 || p.stride_w > 1) &&
+            cmajor_fill_plan(p, sm_count, 0, 1, &w)) {
+            const long long rows_px =
+                (long long)(w.m_tiles + w.cm_ctas_per_tile - 1) / w.cm_ctas_per_tile * w.cm_unit_px;
+            const int n_ct = (p.c_out + kTcBlockM - 1) / kTcBlockM;
+            const long long chunks = (p.m + 31) / 32 * n_ct;
+            const long long swap_tiles_all = (p.m + 255) / 256 * n_ct;
+            const long long boxes =
+                std::min(swap_boxes_balanced(p.m, n_ct, (int)std::min<long long>(chunks, sm_count)),
+                         swap_boxes_whole(swap_tiles_all, (int)std::min<long long>(swap_tiles_all, sm_count)));
+            if (rows_px <= boxes * kTcBlockM) {
                 *out = w;
                 return 0;
             }
         }
-        if (q.wres == 1 || q.row_boxes == 1) return -1;
     }
     if (t.swap_ab) {
         // The channel-major tile is 128 channels x up to 256 pixels.  Whole 256-pixel

@@ -129,3 +129,27 @@ def test_channel_major_other_activations(capi, activation):
     ref = oracle.conv_bn_act(inp.x_bits, inp.w_bits, inp.gamma, inp.beta, inp.mean, inp.var, inp.eps,
                              sh.stride, sh.pad, activation=activation)
     _check(y, ref, f"down ({activation}, row boxes)")
+
+
+def test_x_modes_on_the_same_buffers(capi):
+    """A 1x1 layer's matrix-row units and its im2col units, on the same x, w and y one after
+    another: the two kinds of x tensor map have the same pixels per unit here, and each call
+    must get its own kind (an im2col load issued with a tiled map is an illegal instruction)."""
+    n, h, w, c, k = 2, 40, 40, 64, 64
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    matrix = capi.plan_request(n, h, w, c, k, 1, 1, 1, 0, sms, row_boxes=1, weights_resident=1)
+    im2col = capi.plan_request(n, h, w, c, k, 1, 1, 1, 0, sms, row_boxes=0, weights_resident=1)
+    assert matrix["row_boxes"] == 1 and im2col["row_boxes"] == 0
+    assert matrix["block_m"] == im2col["block_m"], (matrix, im2col)  # same pixels per unit
+    shape = LayerShape("modes", n, h, w, c, k, 1, 1, 1, 0)
+    inp, x, wt, scale, bias = _inputs(capi, shape, seed=733)
+    ref = oracle.conv_bn_silu(inp.x_bits, inp.w_bits, inp.gamma, inp.beta, inp.mean, inp.var, inp.eps, 1, 0)
+    y = torch.empty((n, h, w, k), dtype=torch.bfloat16, device=x.device)
+    order = [{"row_boxes": 1, "weights_resident": 1}, {"row_boxes": 0, "weights_resident": 1},
+             {"row_boxes": 1, "weights_resident": 0}, {"row_boxes": 0, "weights_resident": 1}, {}]
+    for req in order:
+        y.fill_(float("nan"))
+        capi.forward_request(x, wt, scale, bias, 1, 0, y=y, **req)
+        torch.cuda.synchronize()
+        capi.check()
+        _check(y, ref, f"x mode {req}")

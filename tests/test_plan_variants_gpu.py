@@ -109,3 +109,50 @@ def test_stream_k_plans_of_different_layouts_share_one_workspace(capi):
         capi.check()
         got = bf16_bits_to_f32(torch_bf16_to_bits(y)).astype(np.float64)
         assert np.all(np.abs(got - ref) <= bound), ov
+
+
+MULTI_TILE_CASES = [
+    # Several pixel tiles per CTA, and tiles whose epilogue warps hold chunks past the last
+    # output channel next to live ones: such a chunk is neither staged nor stored, and the
+    # staging buffers of the live chunks (reused by the CTA's next tile) stay consistent.
+    ("n256_cout64", LayerShape("mt", 4, 160, 160, 16, 64, 3, 3, 1, 1),
+     {"swap_ab": 0, "stream_k": 0, "pair": 0, "block_n": 256}),
+    ("n128_cout80", LayerShape("mt", 4, 160, 160, 16, 80, 3, 3, 1, 1),
+     {"swap_ab": 0, "stream_k": 0, "pair": 0, "block_n": 128}),
+    ("n256_sk_cout64", LayerShape("mt", 4, 160, 160, 16, 64, 3, 3, 1, 1),
+     {"swap_ab": 0, "stream_k": 1, "pair": 0, "block_n": 256}),
+    # stream-K with tiles narrower than 128 channels: the combining piece's prefetch of its
+    # partner's partial sums covers only the warp's own 32 or 16 accumulator columns
+    ("n64_sk", LayerShape("mt", 4, 80, 80, 128, 64, 3, 3, 1, 1),
+     {"swap_ab": 0, "stream_k": 1, "pair": 0, "block_n": 64}),
+    ("n32_sk_ragged", LayerShape("mt", 4, 80, 80, 128, 48, 3, 3, 1, 1),
+     {"swap_ab": 0, "stream_k": 1, "pair": 0, "block_n": 32}),
+    ("swap_tiles_ragged", LayerShape("mt", 3, 100, 100, 64, 200, 3, 3, 1, 1), {"swap_ab": 1, "balanced": 0}),
+]
+
+
+@pytest.mark.parametrize("name,shape,overrides", MULTI_TILE_CASES, ids=[c[0] for c in MULTI_TILE_CASES])
+def test_multi_tile_ctas_match_oracle(capi, name, shape, overrides):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = capi.plan_request(shape.n, shape.h, shape.w, shape.c, shape.k, shape.r, shape.s, shape.stride,
+                             shape.pad, sms, **overrides)
+    assert plan["tiles"] > plan["grid"], plan  # some CTA runs more than one tile
+    dev = torch.device("cuda:0")
+    inp = make_layer_inputs(shape, seed=89)
+    x = bits_to_torch_bf16(inp.x_bits).to(dev)
+    w = bits_to_torch_bf16(inp.w_bits).to(dev)
+    g, b, m, v = (torch.from_numpy(a).to(dev) for a in (inp.gamma, inp.beta, inp.mean, inp.var))
+    scale, bias = capi.fold(g, b, m, v, inp.eps)
+    ref = oracle.conv_bn_silu(inp.x_bits, inp.w_bits, inp.gamma, inp.beta, inp.mean, inp.var, inp.eps,
+                              shape.stride, shape.pad)
+    bound = 1e-2 + 1e-2 * np.abs(ref)
+    y = torch.empty(ref.shape, dtype=torch.bfloat16, device=dev)
+    for rep in range(3):  # a race shows on some runs only
+        y.fill_(float("nan"))
+        capi.forward_request(x, w, scale, bias, shape.stride, shape.pad, y=y, **overrides)
+        torch.cuda.synchronize()
+        capi.check()
+        got = bf16_bits_to_f32(torch_bf16_to_bits(y)).astype(np.float64)
+        err = np.abs(got - ref)
+        assert np.all(np.isfinite(got)), (name, rep)
+        assert np.all(err <= bound), (name, rep, int((err > bound).sum()), float((err - bound).max()))
