@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
-            dev::mbar_init(dev::smem_u32(&full[i]), 1);
+            dev::mbar_init(dev::smem_u32(&full[i]), WRES ? 1 : 2);  // one arrival per producer
             dev::mbar_init(dev::smem_u32(&empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -222,8 +222,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     dev::grid_dependency_wait();
     dev::grid_dependents_launch();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || (!WRES && warp == 2)) {
+        // ------------------------------------------------------------ producers
+        // Streamed weights: warp 0 loads the x boxes and warp 2 the weight tiles, each
+        // arriving on the stage's full barrier with its own byte count (two issuing threads
+        // keep more of the load path busy than one).  Resident weights: warp 0 alone.
+        const bool loads_w = warp == 2;
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -278,12 +282,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (!(ok = wait_empty())) break;
                     const uint32_t f_bar = dev::smem_u32(&full[stage]);
                     const uint32_t dst = dev::smem_u32(sm_stage + stage * a.stage_bytes);
-                    dev::mbar_arrive_expect_tx(f_bar, x_bytes + (WRES ? 0u : 128u * BK * 2u));
-                    if constexpr (!WRES)
+                    if (loads_w) {
+                        dev::mbar_arrive_expect_tx(f_bar, 128u * BK * 2u);
                         dev::tma_load_3d(dst, &tm_w, f_bar, cc * BK, r * a.s + s, ct * 128);
-                    if constexpr (XMODE == kXMatrix) {
+                    } else if constexpr (XMODE == kXMatrix) {
+                        dev::mbar_arrive_expect_tx(f_bar, x_bytes);
                         tma_load_2d_rows(dst + (uint32_t)b_off, &tm_x, f_bar, cc * BK, u.p0);
                     } else if constexpr (XMODE == kXRows) {
+                        dev::mbar_arrive_expect_tx(f_bar, x_bytes);
                         // Input pixel stride*ow - pad + s of row stride*oh - pad + r: in the
                         // (stride*C, W/stride, H, N) view, element (s - pad) mod stride of
                         // "pixel" ow + floor((s - pad) / stride).
@@ -293,6 +299,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tma_load_4d(dst + (uint32_t)b_off, &tm_x, f_bar, half * a.c + cc * BK, q,
                                     u.oh0 * a.stride_h - a.pad_h + r, u.img);
                     } else {
+                        dev::mbar_arrive_expect_tx(f_bar, x_bytes);
                         dev::tma_load_im2col_4d(dst + (uint32_t)b_off, &tm_x, f_bar, cc * BK, corner_w, corner_h, img,
                                                 (uint16_t)s, (uint16_t)r);
                     }

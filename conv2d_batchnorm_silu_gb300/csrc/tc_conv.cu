@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            dev::mbar_init(dev::smem_u32(&full[i]), 1);
+            dev::mbar_init(dev::smem_u32(&full[i]), 2);  // the two producers' arrivals
             dev::mbar_init(dev::smem_u32(&empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -376,8 +376,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     dev::grid_dependency_wait();
     dev::grid_dependents_launch();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ producers
+        // Two issuing threads: warp 0 loads the x operand (im2col boxes), warp 2 the weight
+        // tile; each arrives on the stage's full barrier with its own byte count.  One thread
+        // issuing every box left the loads short of what the tensor pipe consumes.
+        const bool loads_w = warp == 2;
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -421,30 +425,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t f_bar = dev::smem_u32(&full[stage]);
                     if constexpr (PAIR) {
                         // Both CTAs' bytes complete on the even CTA's full barrier.
-                        if (rank == 0) dev::mbar_arrive_expect_tx(f_bar, 2 * (C::A_BYTES + C::B_BYTES));
                         const uint32_t f0 = full0 + (uint32_t)(stage * 8);
-                        dev::tma_load_im2col_4d_pair(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_x, f0,
-                                                     cc * BK, corner_w, corner_h, img, (uint16_t)s,
-                                                     (uint16_t)r);
-                        dev::tma_load_3d_pair(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f0, cc * BK,
-                                              r * a.s + s, n0 + rank * (BN / 2));
+                        if (loads_w) {
+                            if (rank == 0) dev::mbar_arrive_expect_tx(f_bar, 2 * C::B_BYTES);
+                            dev::tma_load_3d_pair(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f0, cc * BK,
+                                                  r * a.s + s, n0 + rank * (BN / 2));
+                        } else {
+                            if (rank == 0) dev::mbar_arrive_expect_tx(f_bar, 2 * C::A_BYTES);
+                            dev::tma_load_im2col_4d_pair(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_x, f0,
+                                                         cc * BK, corner_w, corner_h, img, (uint16_t)s,
+                                                         (uint16_t)r);
+                        }
                     } else if constexpr (SWAP) {
-                        dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES + (two_boxes ? 2 : 1) * C::BM * BK * 2);
-                        dev::tma_load_3d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_w, f_bar,
-                                         cc * BK, r * a.s + s, n0);
-                        const uint32_t bdst = dev::smem_u32(sm_b + stage * C::B_STRIDE);
-                        dev::tma_load_im2col_4d(bdst, &tm_x, f_bar, cc * BK, corner_w, corner_h, img,
-                                                (uint16_t)s, (uint16_t)r);
-                        if (two_boxes)
-                            dev::tma_load_im2col_4d(bdst + C::BM * BK * 2, &tm_x, f_bar, cc * BK, corner_w1,
-                                                    corner_h1, img1, (uint16_t)s, (uint16_t)r);
+                        if (loads_w) {
+                            dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES);
+                            dev::tma_load_3d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_w, f_bar,
+                                             cc * BK, r * a.s + s, n0);
+                        } else {
+                            dev::mbar_arrive_expect_tx(f_bar, (two_boxes ? 2 : 1) * C::BM * BK * 2);
+                            const uint32_t bdst = dev::smem_u32(sm_b + stage * C::B_STRIDE);
+                            dev::tma_load_im2col_4d(bdst, &tm_x, f_bar, cc * BK, corner_w, corner_h, img,
+                                                    (uint16_t)s, (uint16_t)r);
+                            if (two_boxes)
+                                dev::tma_load_im2col_4d(bdst + C::BM * BK * 2, &tm_x, f_bar, cc * BK, corner_w1,
+                                                        corner_h1, img1, (uint16_t)s, (uint16_t)r);
+                        }
                     } else {
-                        dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES + C::B_BYTES);
-                        dev::tma_load_im2col_4d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_x, f_bar,
-                                                cc * BK, corner_w, corner_h, img, (uint16_t)s,
-                                                (uint16_t)r);
-                        dev::tma_load_3d(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f_bar,
-                                         cc * BK, r * a.s + s, n0);
+                        if (loads_w) {
+                            dev::mbar_arrive_expect_tx(f_bar, C::B_BYTES);
+                            dev::tma_load_3d(dev::smem_u32(sm_b + stage * C::B_STRIDE), &tm_w, f_bar,
+                                             cc * BK, r * a.s + s, n0);
+                        } else {
+                            dev::mbar_arrive_expect_tx(f_bar, C::A_BYTES);
+                            dev::tma_load_im2col_4d(dev::smem_u32(sm_a + stage * C::A_STRIDE), &tm_x, f_bar,
+                                                    cc * BK, corner_w, corner_h, img, (uint16_t)s,
+                                                    (uint16_t)r);
+                        }
                     }
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
