@@ -47,7 +47,8 @@ namespace {
 constexpr uint64_t kGatherTimeoutNs = 2000000000ull;
 constexpr int kGatherThreads = kGatherBlockThreads;  // 4 epilogue + 4 builder warps + the MMA warp
 constexpr int kGatherR = 3, kGatherS = 3;
-constexpr int kStageCap = 40960;       // bytes of staged input rows per pass
+constexpr int kStageCap = 32768;       // bytes of staged input rows per pass
+constexpr int kStageSlack = 64;        // bytes after the staging buffer that tap reads may touch
 constexpr int kBulkPiece = 16384;      // bytes per cp.async.bulk copy
 
 struct GatherArgs {
@@ -65,6 +66,12 @@ struct GatherArgs {
     const __nv_bfloat16 *residual;  // nullable: bf16 [m][c_out] added after the activation
 };
 
+// CTAs resident per SM: three for 3 input channels (a 64-byte operand row: three CTAs' shared
+// memory fits, and the kernel fits 75 registers a thread without spilling), two otherwise.
+// More CTAs per SM means fewer 128-pixel tiles per CTA, whose A rows each CTA's builders
+// write one tile after another.
+__host__ __device__ constexpr int kGatherCtasPerSm(int c) { return c == 3 ? 3 : 2; }
+
 template <int C, int N>
 struct GatherCfg {
     static constexpr int TAPS = kGatherR * kGatherS * C;
@@ -74,7 +81,7 @@ struct GatherCfg {
     static constexpr int A_BYTES = 128 * ROW;
     static constexpr int B_BYTES = ((N * ROW + 1023) / 1024) * 1024;
     static constexpr int TMEM_COLS = 2 * N <= 32 ? 32 : (2 * N <= 64 ? 64 : 128);  // power of two
-    static constexpr int SMEM = 1024 + STAGES * A_BYTES + B_BYTES + kStageCap + 256;  // + barriers
+    static constexpr int SMEM = 1024 + STAGES * A_BYTES + B_BYTES + kStageCap + kStageSlack + 256;  // + barriers
     static_assert(TAPS <= 64, "the receptive field must fit one 128-byte row");
     static_assert(N % 16 == 0 && N >= 16 && N <= 64, "UMMA N for M=128, epilogue width");
 };
@@ -148,7 +155,7 @@ __host__ __device__ inline int pass_end(int ps, int p_end, int wo, int pass_rows
 }
 
 template <int C, int N>
-__global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kernel(const GatherArgs a)
+__global__ void __launch_bounds__(kGatherThreads, kGatherCtasPerSm(C)) tc_gather_conv_bn_silu_kernel(const GatherArgs a)
 {
     using G = GatherCfg<C, N>;
     constexpr int KPAD = G::KPAD;
@@ -160,7 +167,7 @@ __global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kern
     uint8_t *sm_a = smem;
     uint8_t *sm_b = sm_a + STAGES * G::A_BYTES;
     uint8_t *sm_x = sm_b + G::B_BYTES;  // 1024-aligned
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm_x + kStageCap);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm_x + kStageCap + kStageSlack);
     uint64_t *full = bars;
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
@@ -198,13 +205,18 @@ __global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kern
     __syncthreads();
     dev::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    dev::grid_dependency_wait();
-    dev::grid_dependents_launch();
-
     // This CTA's equal share of the output pixels, processed in passes of at most
     // pass_rows output rows (one pass when the share's input rows fit the staging buffer).
+    // The share and the first pass's rows and bytes come from the launch arguments alone:
+    // they are worked out before the wait for the preceding kernel, off the critical path.
     int p_begin, p_end;
     cta_share((int)a.m, (int)blockIdx.x, (int)gridDim.x, &p_begin, &p_end);
+    const int pe_first = p_begin < p_end ? pass_end(p_begin, p_end, a.wo, a.pass_rows) : p_end;
+    const RowSpan rs_first = pass_rows(p_begin, p_begin < p_end ? pe_first : p_begin + 1, a.howo, a.wo, a.h,
+                                       a.stride_h, a.pad_h);
+    const PassBytes pb_first = pass_bytes(rs_first, a.row_bytes);
+    dev::grid_dependency_wait();
+    dev::grid_dependents_launch();
 
     if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ builders
@@ -218,9 +230,9 @@ __global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kern
         const char *xg = reinterpret_cast<const char *>(a.x);
         int pass = 0;
         for (int ps = p_begin, pe; ps < p_end && ok; ps = pe, ++pass) {
-            pe = pass_end(ps, p_end, a.wo, a.pass_rows);
-            const RowSpan rs = pass_rows(ps, pe, a.howo, a.wo, a.h, a.stride_h, a.pad_h);
-            const PassBytes pb = pass_bytes(rs, a.row_bytes);
+            pe = pass == 0 ? pe_first : pass_end(ps, p_end, a.wo, a.pass_rows);
+            const RowSpan rs = pass == 0 ? rs_first : pass_rows(ps, pe, a.howo, a.wo, a.h, a.stride_h, a.pad_h);
+            const PassBytes pb = pass == 0 ? pb_first : pass_bytes(rs, a.row_bytes);
             if (warp == 4) {
                 // Builder warp 4 stages the pass's rows, once every builder warp is done
                 // reading the previous pass's: the unaligned head and tail (under 16 bytes
@@ -237,6 +249,21 @@ __global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kern
                     if (lane == 0 && !*abort_flag) gather_error(kErrTimeoutProducer, abort_flag);
                     ok = false;
                 } else {
+                    // The body's copies go out first (the barrier learns their byte count without
+                    // an arrival); the head and tail loads, which wait for global memory, follow, and
+                    // lane 0's arrival after the warp has stored them releases the whole pass.
+                    const uint32_t xb = dev::smem_u32(xfull);
+                    if (lane == 0) {
+                        const long long body = pb.b1 - pb.b0;
+                        if (body > 0) {
+                            dev::mbar_expect_tx(xb, (uint32_t)body);
+                            for (long long q = pb.b0; q < pb.b1; q += kBulkPiece) {
+                                const uint32_t len = (uint32_t)(pb.b1 - q < kBulkPiece ? pb.b1 - q : kBulkPiece);
+                                dev::bulk_load(dev::smem_u32(sm_x + (q - pb.a0)), xg + q, len, xb);
+                            }
+                            x_pending = true;
+                        }
+                    }
                     const long long head_end = pb.b0 < pb.ge ? pb.b0 : pb.ge;
                     const long long tail_beg = pb.b1 > head_end ? pb.b1 : head_end;
                     const int nhead = (int)((head_end - pb.gs) / 2), ntail = (int)((pb.ge - tail_beg) / 2);
@@ -245,20 +272,7 @@ __global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kern
                         dev::sts_u16(dev::smem_u32(sm_x) + (uint32_t)(o - pb.a0),
                                      __ldg(reinterpret_cast<const unsigned short *>(xg + o)));
                     __syncwarp();  // the plain writes happen before lane 0's arrive, which releases them
-                    if (lane == 0) {
-                        const uint32_t xb = dev::smem_u32(xfull);
-                        const long long body = pb.b1 - pb.b0;
-                        if (body > 0) {
-                            dev::mbar_arrive_expect_tx(xb, (uint32_t)body);
-                            for (long long q = pb.b0; q < pb.b1; q += kBulkPiece) {
-                                const uint32_t len = (uint32_t)(pb.b1 - q < kBulkPiece ? pb.b1 - q : kBulkPiece);
-                                dev::bulk_load(dev::smem_u32(sm_x + (q - pb.a0)), xg + q, len, xb);
-                            }
-                            x_pending = true;
-                        } else {
-                            dev::mbar_arrive(xb);
-                        }
-                    }
+                    if (lane == 0) dev::mbar_arrive(xb);
                 }
             }
             if (!dev::mbar_wait_bounded(dev::smem_u32(xfull), xphase, abort_flag, kGatherTimeoutNs)) {
@@ -294,28 +308,41 @@ __global__ void __launch_bounds__(kGatherThreads, 2) tc_gather_conv_bn_silu_kern
                     const int ow = rem - oh * a.wo;
                     // Staged row index of input row ih of this pixel's image: row0 + ih.
                     const int row0 = (int)((long long)img * a.h - rs.first);
-                    int coff[kGatherS];
+                    // Input pixels iw0, iw0 + 1, iw0 + 2 of a row (the three taps s) are 6C
+                    // contiguous bytes of the staged row: read as the aligned 32-bit words that
+                    // cover them (two-byte aligned start: a funnel shift of 0 or 16 bits), a third
+                    // of the load instructions of one two-byte load per value.  A tap in the
+                    // padding reads neighbouring bytes (the weight tile before the staging buffer,
+                    // the slack after it: at most 2 * 2C + 2 bytes before a row, 4 * NW after its
+                    // last tap) and is zeroed below.
+                    const int iw0 = ow * a.stride_w - a.pad_w;
                     bool cin[kGatherS];
 #pragma unroll
-                    for (int s = 0; s < kGatherS; ++s) {
-                        const int iw = ow * a.stride_w - a.pad_w + s;
-                        cin[s] = iw >= 0 && iw < a.w_in;
-                        coff[s] = iw * (C * 2);
-                    }
+                    for (int s = 0; s < kGatherS; ++s) cin[s] = iw0 + s >= 0 && iw0 + s < a.w_in;
+                    constexpr int NW = (6 * C + 5) / 4;  // words covering 6C bytes from a two-byte offset
+                    uint32_t in_mask = 0;
 #pragma unroll
                     for (int r = 0; r < kGatherR; ++r) {
                         const int ih = oh * a.stride_h - a.pad_h + r;
                         const bool rin = ih >= 0 && ih < a.h;
-                        const uint32_t rp = xs + (uint32_t)(rin ? (row0 + ih) * a.row_bytes : 0);
+                        const uint32_t start =
+                            rin ? xs + (uint32_t)((row0 + ih) * a.row_bytes + iw0 * (C * 2)) : xs;
+                        const uint32_t wa = start & ~3u, sh = (start & 2u) * 8u;
+                        uint32_t w[NW];
 #pragma unroll
-                        for (int s = 0; s < kGatherS; ++s) {
-                            const bool in = rin && cin[s];
+                        for (int j = 0; j < NW; ++j) w[j] = dev::lds_u32(wa + 4u * j);
 #pragma unroll
-                            for (int c = 0; c < C; ++c)
-                                v[(r * kGatherS + s) * C + c] =
-                                    in ? (unsigned short)dev::lds_u16(rp + (uint32_t)(coff[s] + c * 2)) : (unsigned short)0;
+                        for (int s = 0; s < kGatherS; ++s) in_mask |= (rin && cin[s]) ? 1u << (r * kGatherS + s) : 0u;
+#pragma unroll
+                        for (int k = 0; k < kGatherS * C; ++k) {
+                            const int j = k / 2, j1 = k / 2 + 1 < NW ? k / 2 + 1 : NW - 1;
+                            const uint32_t two = __funnelshift_r(w[j], w[j1], sh);
+                            v[r * kGatherS * C + k] = (unsigned short)((k & 1) ? two >> 16 : two & 0xffffu);
                         }
                     }
+#pragma unroll
+                    for (int q = 0; q < G::TAPS; ++q)
+                        if (!((in_mask >> (q / C)) & 1u)) v[q] = 0;
                 } else {
 #pragma unroll
                     for (int q = 0; q < G::TAPS; ++q) v[q] = 0;
@@ -593,7 +620,10 @@ bool gather_supported(const ConvProblem &p)
 {
     if (p.m > 0x7fffffffLL - 128) return false;
     if (p.out_fp8) return false;  // the bf16 output only (the direct kernel writes fp8)
-    const bool shape = p.r == kGatherR && p.s == kGatherS && (p.c == 1 || p.c == 3 || p.c == 4);
+    // Padding of at most filter - 1: every output row reads at least one input row, which the
+    // pass bounds (pass_rows) rely on, and the tap reads stay within the staging slack.
+    const bool shape = p.r == kGatherR && p.s == kGatherS && (p.c == 1 || p.c == 3 || p.c == 4) &&
+                       p.pad_h >= 0 && p.pad_h <= kGatherR - 1 && p.pad_w >= 0 && p.pad_w <= kGatherS - 1;
     if (!shape || p.c_out < 1 || p.c_out > 64) return false;
     // A single output pixel's rows must fit the staging buffer.
     return (long long)kGatherR * p.w_in * p.c * 2 + 32 <= kStageCap;
@@ -603,7 +633,7 @@ bool gather_plan(const ConvProblem &p, int sm_count, GatherPlan *out)
 {
     if (!gather_supported(p)) return false;
     const long long tiles = (p.m + 127) / 128;
-    const int grid = (int)std::min<long long>(tiles, 2LL * sm_count);
+    const int grid = (int)std::min<long long>(tiles, (long long)kGatherCtasPerSm(p.c) * sm_count);
     // The pass size walks every CTA's passes once per shape; later calls hit this cache.
     struct Entry {
         long long m;
@@ -644,7 +674,8 @@ bool gather_plan(const ConvProblem &p, int sm_count, GatherPlan *out)
     out->block_n = n;
     out->block_k = kpad;
     out->stages = stages;
-    out->smem_bytes = 1024 + stages * 128 * kpad * 2 + (n * kpad * 2 + 1023) / 1024 * 1024 + kStageCap + 256;
+    out->smem_bytes =
+        1024 + stages * 128 * kpad * 2 + (n * kpad * 2 + 1023) / 1024 * 1024 + kStageCap + kStageSlack + 256;
     return true;
 }
 

@@ -68,9 +68,9 @@ def test_plan_for_the_five_layers(lib):
         p = lib.plan(sh.n, sh.h, sh.w, sh.c, sh.k, sh.r, sh.s, sh.stride, sh.pad, "auto", 152)
         assert p["algo"] == expect_algo[name], (name, p)
         if name == "stem":
-            # thin-input tensor-core kernel: K = 27 zero-padded to 32, two CTAs per SM
+            # thin-input tensor-core kernel: K = 27 zero-padded to 32, three CTAs per SM
             assert p["block_m"] == 128 and p["block_n"] == 16 and p["block_k"] == 32
-            assert p["tiles"] == 800 and p["grid"] == 304 and p["smem_bytes"] <= 113 * 1024
+            assert p["tiles"] == 800 and p["grid"] == 456 and 3 * (p["smem_bytes"] + 1024) <= 228 * 1024
             continue
         if name in ("down", "pointwise"):
             # channel-major tiles, x in boxes of whole output rows (the 1x1 layer: of its
@@ -107,6 +107,12 @@ def test_plan_rejects_what_tcgen05_cannot_run(lib):
     with pytest.raises(lib.CbsError):
         lib.plan(1, 64, 64, 16, 12, 3, 3, 1, 1, "tcgen05", 152)  # c_out % 8 != 0
     assert lib.plan(1, 64, 64, 3, 16, 3, 3, 2, 1, "direct", 152)["algo"] == "direct"
+    # the thin-input kernel takes a padding of at most 2 (every output row then reads an
+    # input row); a larger one goes to the direct kernel
+    assert lib.plan(1, 64, 64, 3, 16, 3, 3, 1, 2, "tcgen05", 152)["algo"] == "tcgen05"
+    with pytest.raises(lib.CbsError):
+        lib.plan(1, 64, 64, 3, 16, 3, 3, 1, 3, "tcgen05", 152)
+    assert lib.plan(1, 64, 64, 3, 16, 3, 3, 1, 3, "auto", 152)["algo"] == "direct"
 
 
 def test_invalid_arguments_return_status_without_gpu(lib):

@@ -41,7 +41,7 @@ CASES = [
     (2, 50, 50, 3, 16, 3, 0),       # stride 3
     (1, 30, 30, 1, 48, 2, 1),       # N = 48
     (2, 33, 17, 4, 40, 1, 0),       # c = 4 (K 36 -> 64), c_out between N widths
-    (1, 12, 2000, 3, 16, 1, 1),     # 12 KB rows: one output row per staging pass
+    (1, 12, 1800, 3, 16, 1, 1),     # 10.8 KB rows, the widest that fit: one output row per staging pass
     (4, 64, 1500, 3, 16, 1, 1),     # 9 KB rows: several passes per CTA
     (8, 640, 640, 3, 16, 2, 1),     # a batch of YOLO stems: shares of 2695 pixels, passes of 4 rows
 ]
