@@ -215,12 +215,13 @@ def device_uuid(dev_index: int) -> str | None:
         return None
 
 
-# The sources the tensor-core implicit-GEMM kernel (the dominant layer's) is built from.
-TC_KERNEL_SOURCES = ("tc_conv.cu", "ptx.cuh", "epilogue.cuh", "cbs_internal.h")
+# The sources of the tensor-core kernels (the dominant layer's and the others' whose DRAM
+# counters profiles/dram_traffic.json records).
+TC_KERNEL_SOURCES = ("tc_conv.cu", "tc_cmajor.cu", "tc_gather.cu", "ptx.cuh", "epilogue.cuh", "cbs_internal.h")
 
 
 def kernel_source_sha(names=TC_KERNEL_SOURCES) -> str:
-    """Hash of the tensor-core kernel's sources: DRAM counters recorded for it in
+    """Hash of the tensor-core kernels' sources: DRAM counters recorded for them in
     profiles/dram_traffic.json are used only while the hash still matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "conv2d_batchnorm_silu_gb300", "csrc")
