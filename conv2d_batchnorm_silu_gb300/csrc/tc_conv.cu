@@ -660,49 +660,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int slot = (u.kb > 0 ? vb - 1 : vb) * (PAIR ? 2 : 1) + rank;
             float4 *part = a.stream_k ? reinterpret_cast<float4 *>(a.partial) + (size_t)slot * (32 * BN)
                                       : nullptr;
-            // When the combining piece is this worker's last unit, the other accumulator
-            // buffer stays idle during its K loop: the partner's partial sums are loaded
-            // into it then, so that the final epilogue reads them from tensor memory.
-            bool prefetched = false;
-            if (combine) {
-                WorkIter peek = wi;
-                WorkUnit q;
-                if (!peek.next(a, q)) {
-                    int got = 1;
-                    if (lane == 0)
-                        got = wait_flag_bounded(a.flags + slot * kTcFlagsPerSlot + ep, abort_flag, a.wait_ns) ? 1 : 0;
-                    got = __shfl_sync(0xffffffffu, got, 0);
-                    if (!got) {
-                        if (lane == 0 && !*abort_flag) record_error(kErrTimeoutEpilogue, abort_flag);
-                        break;
-                    }
-                    __threadfence();
-                    const uint32_t t_other =
-                        tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)((buf ^ 1) * BN + col_base);
-                    // At most 64 of the warp's columns per pass, never more than it owns.
-                    constexpr int PC = C::EPI_COLS < 64 ? C::EPI_COLS : 64;
-                    static_assert(PC % 16 == 0 && C::EPI_COLS % PC == 0, "whole 16-column stores");
-#pragma unroll 1
-                    for (int c0 = 0; c0 < C::EPI_COLS; c0 += PC) {
-                        uint32_t pv[PC];
-#pragma unroll
-                        for (int g = 0; g < PC / 4; ++g) {
-                            const float4 p4 = __ldcg(part + (size_t)((col_base + c0) / 4 + g) * C::BM + row);
-                            pv[4 * g] = __float_as_uint(p4.x);
-                            pv[4 * g + 1] = __float_as_uint(p4.y);
-                            pv[4 * g + 2] = __float_as_uint(p4.z);
-                            pv[4 * g + 3] = __float_as_uint(p4.w);
-                        }
-#pragma unroll
-                        for (int q16 = 0; q16 < PC / 16; ++q16)
-                            dev::tmem_st_32x32b_x16(t_other + (uint32_t)(c0 + 16 * q16), pv + 16 * q16);
-                    }
-                    dev::tmem_st_wait();
-                    __syncwarp();  // every lane has read the partial: the slot is free again
-                    if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 0);
-                    prefetched = true;
-                }
-            }
             // The unit's per-channel scale and bias, read while its K loop still runs: the
             // first touch of these lines otherwise costs an L2 round trip inside the epilogue.
             float swap_hs = 0.f, swap_hb = 0.f;  // channel-major tiles: this thread's channel
@@ -829,7 +786,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int m_tile = PAIR ? 2 * m_unit + rank : m_unit;
             const int n0 = (u.tile - m_unit * a.n_tiles) * BN;
             const int row0 = m_tile * C::BM + ew * 32;  // first output pixel of this warp
-            if (combine && !prefetched) {
+            if (combine) {
                 int got = 1;
                 if (lane == 0)
                     got = wait_flag_bounded(a.flags + slot * kTcFlagsPerSlot + ep, abort_flag, a.wait_ns) ? 1 : 0;
@@ -866,26 +823,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int q = 0; q < EC / 16; ++q)
                     dev::tmem_ld_32x32b_x16(t_lane + (uint32_t)(j * EC + q * 16), v + q * 16);
-                if (prefetched) {
-                    // The partner's partial sums, prefetched into the other accumulator buffer.
-                    uint32_t pv[EC];
-                    const uint32_t t_other = t_lane + (uint32_t)((buf ^ 1) * BN - buf * BN);
+                dev::tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < EC / 16; ++q)
-                        dev::tmem_ld_32x32b_x16(t_other + (uint32_t)(j * EC + q * 16), pv + q * 16);
-                    dev::tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < EC / 16; ++q) {
-                        dev::reg_fence16(v + q * 16);
-                        dev::reg_fence16(pv + q * 16);
-                    }
-#pragma unroll
-                    for (int i = 0; i < EC; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(pv[i]));
-                } else {
-                    dev::tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < EC / 16; ++q) dev::reg_fence16(v + q * 16);
-                }
+                for (int q = 0; q < EC / 16; ++q) dev::reg_fence16(v + q * 16);
                 if (j == C::EPI_COLS / EC - 1) {
                     // The accumulator is in registers: hand the TMEM buffer back to the MMA warp.
                     dev::tc_fence_before_sync();
@@ -906,7 +846,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
                     continue;
                 }
-                if (combine && !prefetched) {
+                if (combine) {
 #pragma unroll
                     for (int q = 0; q < EC / 4; ++q) {
                         const float4 p4 = __ldcg(part + (size_t)((col_base + j * EC) / 4 + q) * C::BM + row);
@@ -1030,7 +970,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 1);
-            } else if (combine && !prefetched) {
+            } else if (combine) {
                 __syncwarp();  // all lanes have read the partial: the slot is free again
                 if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 0);
             }
