@@ -65,6 +65,11 @@ struct TcPlan {
 
 constexpr int kTcBlockM = 128;
 constexpr int kTcThreads = 384;  // producer, MMA, two idle, eight epilogue warps
+// Channel-major kernel of tc_cmajor.cu: producer, MMA, weight producer, one idle warp and
+// twelve epilogue warps (three per TMEM lane quarter: the epilogue, not the loads, paced
+// its units with eight).
+constexpr int kCmEpiWarps = 12;
+constexpr int kCmThreads = 128 + 32 * kCmEpiWarps;
 // Stream-K slot words: a ready flag per epilogue warp.
 constexpr int kTcFlagsPerSlot = 8;
 

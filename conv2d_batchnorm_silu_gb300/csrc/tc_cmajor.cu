@@ -20,9 +20,10 @@
 //     MMAs read their A operand from there; only x streams.  Off: one 128 x BK
 //     weight load per K step next to the x box, the MMAs read both operands
 //     from shared memory, and the accumulators may use all of tensor memory.
-// Warp roles: warp 0 TMA producer, warp 1 MMA issuer (one thread), warps 4..11
-// epilogue (BN multiply/add, activation, bf16, transposed to NHWC through
-// shared memory, TMA stores of 32 channels x 16 pixels).  Accumulators are
+// Warp roles: warp 0 TMA producer of x, warp 2 of the weights, warp 1 MMA issuer
+// (one thread), warps 4..15 epilogue (BN multiply/add, activation, bf16, transposed
+// to NHWC through shared memory, TMA stores of 32 channels x 16 pixels; three warps
+// per TMEM lane quarter, since with two the epilogue, not the K loop, set the pace).  Accumulators are
 // double buffered in TMEM, so the epilogue of one unit runs under the K loop of
 // the next.  Every wait is bounded in time; on a timeout the kernel records an
 // error bit, waits for its own copies in flight, frees TMEM and returns.
@@ -47,7 +48,6 @@ constexpr uint64_t kCmTimeoutNs = 2000000000ull;
 constexpr int kCmMaxStages = 16;
 constexpr int kCmChunk = 16;            // pixels per epilogue chunk (one TMA store of 32 channels)
 constexpr int kCmStgBytes = kCmChunk * 32 * 2;
-constexpr int kCmEpiWarps = 8;
 constexpr int kCmSmemLimit = 232448;
 constexpr int kEpiCmSilu = 0;           // the fused layer's own epilogue
 constexpr int kEpiCmMode = 1;           // the launch's EpiMode, chosen at run time
@@ -163,7 +163,7 @@ struct CmIter {
 };
 
 template <int BK, int EPI, bool WRES, int XMODE>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kCmThreads, 1)
     tc_cmajor_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                      const __grid_constant__ CUtensorMap tm_y, const CmArgs a)
 {
@@ -413,11 +413,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else if (warp >= 4 && warp < 4 + kCmEpiWarps) {
         // ------------------------------------------------------------ epilogue
-        // TMEM lane = output channel, column = pixel.  Warps w and w+4 share lane
-        // quarter w % 4 (32 channels) and take alternate 16-pixel chunks; each thread
-        // owns one channel, transposed to NHWC through shared memory.
+        // TMEM lane = output channel, column = pixel.  Warps w, w + 4 and w + 8 share
+        // lane quarter w % 4 (32 channels) and take every third 16-pixel chunk in turn;
+        // each thread owns one channel, transposed to NHWC through shared memory.
         const int ew = warp & 3;
-        const int half = (warp - 4) >> 2;
+        const int half = (warp - 4) >> 2;  // which of the quarter's warps: 0, 1 or 2
         uint8_t *my_stg = sm_stg + (warp - 4) * 2 * kCmStgBytes;
         const int ch_w0 = ct * 128 + ew * 32;  // warp's first channel
         const int ch = ch_w0 + lane;
@@ -449,12 +449,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 continue;
             }
 #pragma unroll 1
-            for (int j = half; j < nchunks; j += 2) {
+            for (int j = half; j < nchunks; j += kCmEpiWarps / 4) {
                 uint32_t v[kCmChunk];
                 dev::tmem_ld_32x32b_x16(t_lane + (uint32_t)(j * kCmChunk), v);
                 dev::tmem_ld_wait();
                 dev::reg_fence16(v);
-                if (j + 2 >= nchunks) {
+                if (j + kCmEpiWarps / 4 >= nchunks) {
                     // This warp's last chunk is in registers: release the accumulator.
                     dev::tc_fence_before_sync();
                     __syncwarp();
@@ -551,7 +551,7 @@ cudaError_t launch_cm(const ConvProblem &p, const TcPlan &plan, const CmMaps &ma
     a.a_bytes = plan.cm_a_bytes;
     a.epi_mode = p.epi_mode;
     a.wait_ns = p.wait_timeout_ns > 0 ? (unsigned long long)p.wait_timeout_ns : kCmTimeoutNs;
-    return launch_overlapped(kern, dim3((unsigned)plan.grid), dim3(kTcThreads), (size_t)plan.smem_bytes, stream, 1,
+    return launch_overlapped(kern, dim3((unsigned)plan.grid), dim3(kCmThreads), (size_t)plan.smem_bytes, stream, 1,
                              maps.x, maps.w, maps.y, a);
 }
 

@@ -1483,9 +1483,11 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
     const bool short_narrow = p.c_out <= 64 && t.k_iters <= 2;
     // Fewer swap tiles than half the SMs: balanced runs still spread the pixels over
     // every SM, and with K loops of eight steps or more their N = 256-wide MMAs beat
-    // the pixel-major tiles (the sweep's 40x40 and 20x20 layers, up to 512 channels).
+    // the pixel-major tiles (the sweep's 40x40 and 20x20 layers, up to 512 channels;
+    // bneck20's 26 swap tiles by 5-11 %, where 128-wide pixel-major tiles keep a third
+    // of the SMs busy).  Below an eighth of the SMs (the 1x32x32 layer's 4) the two tie.
     const bool swap_small = p.c_out >= 32 && p.c_out <= 512 && !pair_path && !short_narrow && t.k_iters >= 8 &&
-                            swap_tiles >= sm_count / 4 && swap_tiles < sm_count / 2;
+                            swap_tiles >= sm_count / 8 && swap_tiles < sm_count / 2;
     t.swap_ab = ((p.c_out >= 32 && p.c_out <= 256 && !pair_path && !short_narrow && swap_tiles >= sm_count / 2) ||
                  swap_small)
                     ? 1

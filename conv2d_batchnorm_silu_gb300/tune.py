@@ -150,7 +150,7 @@ def sweep(iters: int = 24, shapes=SWEEP, log=sys.stderr) -> list[dict]:
 def _plan_label(pl: dict) -> str:
     if pl["algo"] == "direct":
         return "direct"
-    if pl["threads"] != 384:
+    if pl["threads"] == 288:  # the thin-input kernel's CTA
         return "thin-input"
     if pl.get("row_boxes"):
         return "rows-wres" if pl.get("weights_resident") else "rows"
