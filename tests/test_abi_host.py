@@ -282,7 +282,7 @@ def test_tuning_sweep_variants_are_consistent():
 
 def test_planner_choices_match_the_measured_sweep():
     """The planner's choice for every layer of the threshold sweep (tune.SWEEP) on a
-    152-SM GB300, as the sweep recorded in profiles/planner_sweep_yolo_layers.md measured
+    152-SM GB300, as the committed planner sweep (tune.py on a GB300) measured
     it: a change to the planner's rules changes one of these and calls for the sweep to
     be run again."""
     from conv2d_batchnorm_silu_gb300 import capi, tune
