@@ -441,7 +441,7 @@ static int fill_plan(const cbs::ConvProblem &p, int algo, int sm_count, const cb
         out.stages = t.stages;
         out.tiles = t.m_tiles * t.n_tiles;
         out.grid = t.grid;
-        out.threads = t.cmajor ? cbs::kCmThreads : cbs::kTcThreads;
+        out.threads = t.cmajor ? cbs::kCmThreads : cbs::tc_threads(t.block_n, t.pair != 0);
         out.smem_bytes = t.smem_bytes;
         out.k_iters = t.k_iters;
         out.stream_k = t.stream_k;

@@ -64,14 +64,24 @@ struct TcPlan {
 };
 
 constexpr int kTcBlockM = 128;
-constexpr int kTcThreads = 384;  // producer, MMA, two idle, eight epilogue warps
+// Epilogue warps per TMEM lane quarter of tc_conv.cu's kernel: three on 256-wide 2-CTA pair
+// tiles (the last tile's epilogue runs with no K loop under it, and more warps hide its
+// latency), two from 64 channels, one below.  The CTA has four other warps.
+__host__ __device__ constexpr int tc_epi_warps_per_quarter(int block_n, bool pair)
+{
+    return (pair && block_n == 256) ? 3 : (block_n >= 64 ? 2 : 1);
+}
+__host__ __device__ constexpr int tc_threads(int block_n, bool pair)
+{
+    return 128 + 32 * 4 * tc_epi_warps_per_quarter(block_n, pair);
+}
 // Channel-major kernel of tc_cmajor.cu: producer, MMA, weight producer, one idle warp and
 // twelve epilogue warps (three per TMEM lane quarter: the epilogue, not the loads, paced
 // its units with eight).
 constexpr int kCmEpiWarps = 12;
 constexpr int kCmThreads = 128 + 32 * kCmEpiWarps;
-// Stream-K slot words: a ready flag per epilogue warp.
-constexpr int kTcFlagsPerSlot = 8;
+// Stream-K slot words: a ready flag per epilogue warp (at most 12).
+constexpr int kTcFlagsPerSlot = 16;
 
 // Epilogue geometry of the tensor-core kernel for an N tile of `block_n`
 // channels: `split` warps share each 32-row TMEM lane quarter (each takes

@@ -16,9 +16,11 @@
 //   warp 1      MMA issuer: tcgen05.mma (M=128, N=BN, K=16) into a TMEM
 //               accumulator; two accumulators so the epilogue of tile i
 //               overlaps the K loop of tile i+1.
-//   warps 4..11 epilogue ("The shape of it"): tcgen05.ld of the finished tile
-//               (warps w and w+4 share TMEM lanes 32*(w%4).. and split the
-//               columns), acc*scale + bias, SiLU, bf16 cast, staged through
+//   warps 4..   epilogue ("The shape of it"): tcgen05.ld of the finished tile
+//               (warps w, w+4, ... share TMEM lanes 32*(w%4).. and split the
+//               columns: two per lane quarter from 64 channels, three on the
+//               2-CTA pair tiles, whose last tile's epilogue has no K loop
+//               under it), acc*scale + bias, SiLU, bf16 cast, staged through
 //               swizzled shared memory and written by TMA stores.  x is read once and y
 //               written once; the conv result never goes to memory.
 // Every mbarrier wait is bounded in time; on timeout the kernel records an
@@ -204,17 +206,22 @@ __device__ __forceinline__ bool wait_flag_bounded(const int *flag, const volatil
 }
 
 // B_ROWS: weight (B) rows held per CTA -- BN, or BN/2 when a CTA pair splits them.
-template <int BN, int BK, int B_ROWS = BN>
+template <int BN, int BK, int B_ROWS = BN, bool PAIRED = false>
 struct TcCfg {
     static constexpr int BM = kTcBlockM;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int A_STRIDE = (A_BYTES + 1023) / 1024 * 1024;
     static constexpr int B_STRIDE = (B_BYTES + 1023) / 1024 * 1024;
-    static constexpr int SPLIT = BN >= 64 ? 2 : 1;  // epilogue warps per TMEM lane quarter
-    static constexpr int EPI_COLS = BN / SPLIT;     // columns of the tile one epilogue warp owns
-    static constexpr int EC = EPI_COLS < 32 ? EPI_COLS : 32;  // epilogue columns per chunk
-    static constexpr int EPI_WARPS = 4 * SPLIT;
+    static constexpr int SPLIT = BN >= 64 ? 2 : 1;  // sets the chunk width below
+    static constexpr int EC = BN / SPLIT < 32 ? BN / SPLIT : 32;  // epilogue columns per chunk
+    static constexpr int NCH = BN / EC;                          // chunks across the tile
+    // Epilogue warps per TMEM lane quarter; warp h of a quarter takes the chunks
+    // [h * NCH / WPQ, (h + 1) * NCH / WPQ), at most MAX_OWN of them.
+    static constexpr int WPQ = tc_epi_warps_per_quarter(BN, PAIRED);
+    static constexpr int MAX_OWN = (NCH + WPQ - 1) / WPQ;
+    static constexpr int EPI_WARPS = 4 * WPQ;
+    static constexpr int THREADS = tc_threads(BN, PAIRED);
     static constexpr int STG_BYTES = 32 * EC * 2;  // one warp's staging buffer (32 rows)
     static constexpr int STG_TOTAL = EPI_WARPS * 2 * STG_BYTES;
     static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN;
@@ -227,6 +234,8 @@ struct TcCfg {
     static constexpr int SMEM = 1024 + STAGES * (A_STRIDE + B_STRIDE) + STG_TOTAL + BAR_BYTES;
     static_assert(STAGES >= 2, "shared memory too small for two stages");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
+    static_assert(BN % EC == 0 && NCH >= WPQ, "every epilogue warp owns at least one whole chunk");
+    static_assert(EPI_WARPS <= kTcFlagsPerSlot && THREADS == 128 + 32 * EPI_WARPS, "epilogue warps");
     static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 ||
                       TMEM_COLS == 512,
                   "TMEM allocation must be a power of two >= 32");
@@ -300,7 +309,7 @@ __device__ __forceinline__ void with_epi_mode(int mode, F &&f)
 }
 
 template <int BN, int BK, bool SWAP, bool PAIR, int EPI>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREADS, 1)
     tc_conv_bn_silu_kernel(const __grid_constant__ CUtensorMap tm_x,
                            const __grid_constant__ CUtensorMap tm_w,
                            const __grid_constant__ CUtensorMap tm_y,
@@ -313,7 +322,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // The epilogue mode: a compile-time constant for the fused layer.
     const int emode = EPI == kEpiKindSilu ? (int)kEpiSilu : a.epi_mode;
     constexpr int CG = PAIR ? 2 : 1;  // tcgen05 CTA group
-    using C = TcCfg<BN, BK, PAIR ? BN / 2 : BN>;
+    using C = TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>;
     constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -568,7 +577,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         constexpr int ROW_Y = EC * 2;
         const int ew = warp & 3;          // this warp may access TMEM lanes [32*ew, 32*ew+32)
         const int ep = warp - 4;          // epilogue warp index
-        const int col_base = (ep >> 2) * C::EPI_COLS;  // this warp's columns of the tile
+        // This warp's chunks of a pixel-major tile: `own` chunks from column col_base.
+        const int c_lo = (ep >> 2) * C::NCH / C::WPQ;
+        const int own = ((ep >> 2) + 1) * C::NCH / C::WPQ - c_lo;
+        const int col_base = c_lo * EC;
         uint8_t *my_stg = sm_stg + ep * 2 * C::STG_BYTES;
         int sbuf = 0;
         int lt = 0;
@@ -599,7 +611,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         WorkIter wi(a, vb, vg);
         WorkUnit u;
         // SWAP: a unit's channel tile, first pixel and count of EC-pixel chunks.  The
-        // two warps of a lane quarter take alternate chunks.
+        // warps of a lane quarter take the chunks in turn.
         const int half = ep >> 2;
         auto swap_geometry = [&](const WorkUnit &q, int &nt, int &p0, int &nchunks) {
             if (a.balanced) {
@@ -622,7 +634,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     swap_geometry(q, nt, p0, nchunks);
                     const int chw = nt * C::BM + ew * 32;
                     if (chw < a.c_out) {
-                        for (int j = half; j < nchunks; j += C::SPLIT) {
+                        for (int j = half; j < nchunks; j += C::WPQ) {
                             const int px = p0 + j * EC + lane;  // EC == 32 on this path
                             if (px < a.m) prefetch_l2(a.residual + (size_t)px * a.c_out + chw);
                         }
@@ -633,7 +645,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int c0 = (q.tile - mu * a.n_tiles) * BN + col_base;
                     const int px = mt * C::BM + ew * 32 + lane;
                     if (px < a.m && c0 < a.c_out) {
-                        const int bytes = 2 * (a.c_out - c0 < C::EPI_COLS ? a.c_out - c0 : C::EPI_COLS);
+                        const int bytes = 2 * (a.c_out - c0 < own * EC ? a.c_out - c0 : own * EC);
                         const char *rp = reinterpret_cast<const char *>(a.residual + (size_t)px * a.c_out + c0);
                         for (int b = 0; b < bytes; b += 128) prefetch_l2(rp + b);
                     }
@@ -672,11 +684,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // One prefetch per 16 channels (64 bytes) of each array, so that every 128-byte
                 // line the warp's columns touch is covered whatever the arrays' alignment.
                 const int c0 = (u.tile - (u.tile / a.n_tiles) * a.n_tiles) * BN + col_base;
-                constexpr int NP = (C::EPI_COLS + 15) / 16;
+                constexpr int NP = (C::MAX_OWN * EC + 15) / 16;
                 static_assert(2 * NP <= 32, "one lane per prefetch");
                 if (lane < 2 * NP) {
                     const int c = c0 + (lane % NP) * 16;
-                    if (c < a.c_out) prefetch_l1(lane < NP ? a.scale + c : a.bias + c);
+                    if (c < a.c_out && c < c0 + own * EC) prefetch_l1(lane < NP ? a.scale + c : a.bias + c);
                 }
             }
             int ok = 1;
@@ -713,11 +725,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
                 }
 #pragma unroll 1
-                for (int j = half; j < nchunks; j += C::SPLIT) {
+                for (int j = half; j < nchunks; j += C::WPQ) {
                     // A chunk wholly past the last pixel or channel is skipped (no staging write
                     // without its store: the wait before each write counts one store per chunk).
                     if (p0 + j * EC >= a.m || ch_w0 >= a.c_out) {
-                        if (j + C::SPLIT >= nchunks) {
+                        if (j + C::WPQ >= nchunks) {
                             dev::tc_fence_before_sync();
                             __syncwarp();
                             if (lane == 0) dev::mbar_arrive(dev::smem_u32(&tempty[buf]));
@@ -732,7 +744,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     dev::tmem_ld_wait();
 #pragma unroll
                     for (int q = 0; q < EC / 16; ++q) dev::reg_fence16(v + q * 16);
-                    if (j + C::SPLIT >= nchunks) {
+                    if (j + C::WPQ >= nchunks) {
                         // This warp's last chunk is in registers: release the accumulator.
                         dev::tc_fence_before_sync();
                         __syncwarp();
@@ -800,12 +812,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t t_lane =
                 tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN + col_base);
 #pragma unroll 1
-            for (int j = 0; j < C::EPI_COLS / EC; ++j) {
+            for (int j = 0; j < own; ++j) {
                 // A chunk wholly past the last output channel or pixel is skipped: nothing of it
                 // is stored (nor published), and it must not touch a staging buffer either, since
                 // the wait before each staging write counts one store per staged chunk.
                 if (row0 >= a.m || n0 + col_base + j * EC >= a.c_out) {
-                    if (j == C::EPI_COLS / EC - 1) {
+                    if (j == own - 1) {
                         dev::tc_fence_before_sync();
                         __syncwarp();
                         if (lane == 0) {
@@ -826,7 +838,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 dev::tmem_ld_wait();
 #pragma unroll
                 for (int q = 0; q < EC / 16; ++q) dev::reg_fence16(v + q * 16);
-                if (j == C::EPI_COLS / EC - 1) {
+                if (j == own - 1) {
                     // The accumulator is in registers: hand the TMEM buffer back to the MMA warp.
                     dev::tc_fence_before_sync();
                     __syncwarp();
@@ -1306,7 +1318,7 @@ template <int BN, int BK, bool SWAP, bool PAIR, int EPI>
 cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &maps, cudaStream_t stream,
                        void *caller_workspace)
 {
-    using C = TcCfg<BN, BK, PAIR ? BN / 2 : BN>;
+    using C = TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>;
     auto kern = tc_conv_bn_silu_kernel<BN, BK, SWAP, PAIR, EPI>;
     // The shared-memory opt-in is per function and device: done once per device.
     static std::mutex attr_mu;
@@ -1358,31 +1370,31 @@ cudaError_t launch_cfg(const ConvProblem &p, const TcPlan &plan, const TcMaps &m
         a.flags = static_cast<int *>(ws);
         a.partial = reinterpret_cast<float *>(static_cast<char *>(ws) + flag_region);
     }
-    return launch_overlapped(kern, dim3((unsigned)plan.grid), dim3(kTcThreads), (size_t)C::SMEM, stream,
+    return launch_overlapped(kern, dim3((unsigned)plan.grid), dim3(C::THREADS), (size_t)C::SMEM, stream,
                              PAIR ? 2 : 1, maps.x, maps.w, maps.y, maps.r, a);
 }
 
 }  // namespace
 
-static int staging_bytes(int block_n)
+static int staging_bytes(int block_n, int pair)
 {
     int split = 1, ec = 16;
     tc_epilogue_geometry(block_n, &split, &ec);
-    return 4 * split * 2 * 32 * ec * 2;
+    return 4 * tc_epi_warps_per_quarter(block_n, pair != 0) * 2 * 32 * ec * 2;
 }
 
 int tc_smem_bytes(int block_n, int block_k, int stages, int pair)
 {
     const int a = (kTcBlockM * block_k * 2 + 1023) / 1024 * 1024;
     const int b = ((pair ? block_n / 2 : block_n) * block_k * 2 + 1023) / 1024 * 1024;
-    return 1024 + stages * (a + b) + staging_bytes(block_n) + 512;
+    return 1024 + stages * (a + b) + staging_bytes(block_n, pair) + 512;
 }
 
 static int stages_for(int block_n, int block_k, int pair = 0)
 {
     const int a = (kTcBlockM * block_k * 2 + 1023) / 1024 * 1024;
     const int b = ((pair ? block_n / 2 : block_n) * block_k * 2 + 1023) / 1024 * 1024;
-    const int fit = (232448 - 1024 - staging_bytes(block_n) - 512) / (a + b);
+    const int fit = (232448 - 1024 - staging_bytes(block_n, pair) - 512) / (a + b);
     return fit < 8 ? fit : 8;
 }
 

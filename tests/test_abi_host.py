@@ -90,6 +90,10 @@ def test_plan_for_the_five_layers(lib):
                 assert p["block_n"] == 256 and p["grid"] == 152
                 assert p["cluster"] == 2
                 assert p["workspace_bytes"] >= 150 * 128 * 256 * 4
+                # 2-CTA pair tiles: twelve epilogue warps (three per TMEM lane quarter)
+                assert p["threads"] == 512 and p["stages"] == 5
+            else:
+                assert p["threads"] == (384 if p["block_n"] >= 64 else 256)
             assert p["grid"] <= 152 and (p["balanced"] or p["grid"] <= p["tiles"])
             assert p["smem_bytes"] <= 232448
             assert p["stages"] >= 2
@@ -219,7 +223,7 @@ def test_plan_request_overrides(lib):
     deep = (32, 20, 20, 512, 512, 3, 3, 1, 1)
     assert lib.plan_request(*deep)["cluster"] == 2                       # the planner's own choice
     p = lib.plan_request(*deep, pair=0)
-    assert p["cluster"] == 1 and p["stream_k"] == 1
+    assert p["cluster"] == 1 and p["stream_k"] == 1 and p["threads"] == 384
     p = lib.plan_request(*deep, stream_k=0)
     assert p["stream_k"] == 0 and p["cluster"] == 1 and p["workspace_bytes"] == 0
     p = lib.plan_request(*deep, block_n=128, stream_k=0)
