@@ -34,10 +34,11 @@ __device__ __forceinline__ float silu_from_half(float h)
     return fmaf(h, tanh_approx(h), h);
 }
 
-// z = acc*scale + bias, then SiLU(z), evaluated as SiLU from h = z/2.
+// z = acc*scale + bias, then SiLU(z), evaluated as SiLU from h = z/2.  Halving is exact, so
+// h = 0.5 * fma(acc, scale, bias) is the FMA of the halved operands with one multiply fewer.
 __device__ __forceinline__ float bn_silu(float acc, float scale, float bias)
 {
-    return silu_from_half(fmaf(acc, 0.5f * scale, 0.5f * bias));
+    return silu_from_half(0.5f * fmaf(acc, scale, bias));
 }
 
 __device__ __forceinline__ float epilogue_value(float acc, float scale, float bias, int mode)
