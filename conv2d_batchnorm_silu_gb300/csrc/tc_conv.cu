@@ -812,7 +812,10 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
                     if (lane == 0 && !*abort_flag) record_error(kErrTimeoutEpilogue, abort_flag);
                     break;
                 }
-                __threadfence();
+                // Lane 0's acquire load saw the flag; the warp barrier orders it before every
+                // lane's reads of the partial sums.  (A sequentially consistent GPU-scope fence
+                // here cost ~2 us per combined tile, on the kernel's critical path.)
+                __syncwarp();
             }
             const uint32_t t_lane =
                 tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN + col_base);
@@ -983,8 +986,8 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
                 sbuf ^= 1;
             }
             if (publish) {
-                // Every lane's partial sums are visible GPU-wide before the flag rises.
-                __threadfence();
+                // The warp barrier orders every lane's partial-sum stores before lane 0's
+                // release store of the flag, which makes them visible with it GPU-wide.
                 __syncwarp();
                 if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 1);
             } else if (combine) {
