@@ -696,6 +696,11 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
                     if (c < a.c_out && c < c0 + own * EC) prefetch_l1(lane < NP ? a.scale + c : a.bias + c);
                 }
             }
+            // Stream-K combine: the partner's flag is nearly always raised before this unit's
+            // accumulator is ready.  Reading it now, while the warp waits anyway, keeps the
+            // load's L2 round trip (~1 us at the end of the kernel) out of the epilogue.
+            int flag_seen = 0;
+            if (combine && lane == 0) flag_seen = ld_acquire_gpu(a.flags + slot * kTcFlagsPerSlot + ep) != 0;
             int ok = 1;
             if (lane == 0)
                 ok = dev::mbar_wait_bounded(dev::smem_u32(&tfull[buf]), tparity, abort_flag,
@@ -805,15 +810,15 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
             const int row0 = m_tile * C::BM + ew * 32;  // first output pixel of this warp
             if (combine) {
                 int got = 1;
-                if (lane == 0)
+                if (lane == 0 && !flag_seen)
                     got = wait_flag_bounded(a.flags + slot * kTcFlagsPerSlot + ep, abort_flag, a.wait_ns) ? 1 : 0;
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!got) {
                     if (lane == 0 && !*abort_flag) record_error(kErrTimeoutEpilogue, abort_flag);
                     break;
                 }
-                // Lane 0's acquire load saw the flag; the warp barrier orders it before every
-                // lane's reads of the partial sums.  (A sequentially consistent GPU-scope fence
+                // Lane 0's acquire load saw the flag (here or before the accumulator wait); the
+                // warp barrier orders it before every lane's reads of the partial sums.  (A sequentially consistent GPU-scope fence
                 // here cost ~2 us per combined tile, on the kernel's critical path.)
                 __syncwarp();
             }
