@@ -2,7 +2,8 @@
 // tiles, built for the layers that are bound by moving x and y.
 //
 // GEMM view as in tc_conv.cu, transposed: D[channel][pixel] = W[channel][k] *
-// X[pixel][k]^T, K ordered (r, s, c); a CTA owns one 128-channel tile and a
+// X[pixel][k]^T, K laid out (r, s, c) and visited in K steps of one tap x BK
+// channels, the taps running fastest; a CTA owns one 128-channel tile and a
 // sequence of pixel units.  Two choices are template switches, picked per
 // shape by the planner:
 //   - XMODE: how x reaches shared memory.  kXIm2col: one im2col box per K step
@@ -250,14 +251,17 @@ __global__ void __launch_bounds__(kCmThreads, 1)
                 issued |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             };
+            // K step it reads filter tap it % taps of channel chunk it / taps: the taps run
+            // fastest, so a unit's first steps read one chunk of its input rows, not all of them.
+            const int taps = a.k_iters / a.c_chunks;
             if constexpr (WRES) {
                 // The resident weight tile first: one load of 128 channels x BK per K step,
-                // in the K order (r, s, c) of the MMAs.
+                // in the K order of the MMAs.
                 for (int it = 0; it < a.k_iters && ok; ++it) {
                     if (!(ok = wait_empty())) break;
                     const uint32_t f_bar = dev::smem_u32(&full[stage]);
                     dev::mbar_arrive_expect_tx(f_bar, 128 * BK * 2);
-                    const int tap = it / a.c_chunks, cc = it - tap * a.c_chunks;
+                    const int cc = it / taps, tap = it - cc * taps;
                     dev::tma_load_3d(dev::smem_u32(sm_stage + stage * a.stage_bytes), &tm_w, f_bar, cc * BK, tap,
                                      ct * 128);
                     mark_issued();
@@ -304,11 +308,11 @@ __global__ void __launch_bounds__(kCmThreads, 1)
                                                 (uint16_t)s, (uint16_t)r);
                     }
                     mark_issued();
-                    if (++cc == a.c_chunks) {
-                        cc = 0;
-                        if (++s == a.s) {
-                            s = 0;
-                            ++r;
+                    if (++s == a.s) {
+                        s = 0;
+                        if (++r * a.s == taps) {
+                            r = 0;
+                            ++cc;
                         }
                     }
                     next_stage();

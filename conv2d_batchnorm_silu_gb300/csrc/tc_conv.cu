@@ -3,8 +3,9 @@
 //
 // GEMM view ("Fusing an Epilogue", kernels book, section "Three kernels for
 // one operation": convolution as a GEMM on the tensor cores):
-//   M = n*ho*wo output pixels, N = c_out, K = r*s*c, ordered (r, s, c) so that
-//   the KRSC weight tensor is already the K-major B operand.
+//   M = n*ho*wo output pixels, N = c_out, K = r*s*c, laid out (r, s, c) so that
+//   the KRSC weight tensor is already the K-major B operand (the K steps, one
+//   tap x BK channels each, are visited with the taps running fastest).
 //   A[m][k] = x[img][oh*sh - ph + r][ow*sw - pw + s][c], zero outside the image.
 //
 // Per CTA (one per SM, persistent over output tiles of 128 pixels x BN channels):
@@ -1542,9 +1543,12 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
         // tune module).  Tiled boxes move at about 1.5x the rate of im2col boxes but only pay
         // with 64-channel K steps (128-byte box rows):
         //  - 1x1 layers read x as a matrix: matrix-row units won or tied on every such layer;
-        //  - stride-2 layers: whole-row units won where they spread as evenly over the SMs as
-        //    the im2col runs (the busiest CTA's pixels no more than its im2col box pixels), and
-        //    lost by about 10% where they did not (row units come in whole rows only);
+        //  - stride-2 layers of one 64-channel chunk: whole-row units won where they spread as
+        //    evenly over the SMs as the im2col runs (the busiest CTA's pixels no more than its
+        //    im2col box pixels), and lost by about 10% where they did not (row units come in
+        //    whole rows only).  With two or more chunks the im2col runs won (down80: 17.2-17.4
+        //    against 18.2-18.4 us), their taps-fastest K order reading one chunk of the input
+        //    rows over the first nine steps;
         //  - 3x3 stride-1 layers: im2col runs won on every such layer.
         // With 32-channel K steps on a 3x3 filter and a large layer, im2col units with the
         // weights resident in tensor memory won by 6-28%: the weight tile is a third of each
@@ -1561,7 +1565,7 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
             *out = w;
             return 0;
         }
-        if (t.swap_ab && t.block_k == 64 && (p.stride_h > 1 || p.stride_w > 1) &&
+        if (t.swap_ab && t.block_k == 64 && p.c <= 64 && (p.stride_h > 1 || p.stride_w > 1) &&
             cmajor_fill_plan(p, sm_count, 0, 1, &w)) {
             const long long rows_px =
                 (long long)(w.m_tiles + w.cm_ctas_per_tile - 1) / w.cm_ctas_per_tile * w.cm_unit_px;
@@ -1588,11 +1592,13 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
         t.m_tiles = (int)ptiles256;
         t.n_tiles = (p.c_out + kTcBlockM - 1) / kTcBlockM;
         t.tiles = t.m_tiles * t.n_tiles;
-        // Balanced runs when they cut the busiest CTA's im2col boxes (the loads bound
-        // these layers) by a quarter or more: the pointwise layer's 200 tiles put four
-        // boxes per K step on 48 CTAs, equal runs at most three on any.  Smaller gains
-        // were within the noise of the measured sweep (tune module), and the shorter
-        // remainder units cost some of it back.
+        // Balanced runs when they cut the busiest CTA's im2col boxes by a quarter or more
+        // (the pointwise layer's 200 tiles put four boxes per K step on 48 CTAs, equal runs
+        // at most three on any), or when whole tiles leave SMs idle: equal runs then spread
+        // the pixels over every SM (down80's 100 tiles: 17.2-17.4 us balanced against
+        // 18.1-18.5 whole, c2f40's 11.9 against 12.5).  Smaller box gains were within the
+        // noise of the measured sweep (tune module), and the shorter remainder units cost
+        // some of it back.
         const long long chunks = (p.m + 31) / 32 * t.n_tiles;
         const int grid_bal = (int)std::min<long long>(chunks, sm_count);
         const int grid_whole = std::min(t.tiles, sm_count);
@@ -1600,8 +1606,9 @@ int tc_make_plan_request(const ConvProblem &p, int sm_count, const PlanRequest *
         const bool bal_fits = chunks * grid_bal < (1LL << 32);
         if (q.balanced == 1 && !bal_fits) return -1;
         t.balanced = q.balanced >= 0 ? q.balanced
-                                     : (bal_fits && (swap_small || 4 * swap_boxes_balanced(p.m, t.n_tiles, grid_bal) <=
-                                                                       3 * swap_boxes_whole(t.tiles, grid_whole))
+                                     : (bal_fits && (swap_small || t.tiles < sm_count ||
+                                                     4 * swap_boxes_balanced(p.m, t.n_tiles, grid_bal) <=
+                                                         3 * swap_boxes_whole(t.tiles, grid_whole))
                                             ? 1
                                             : 0);
         t.grid = t.balanced ? grid_bal : grid_whole;

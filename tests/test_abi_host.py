@@ -292,7 +292,7 @@ def test_planner_choices_match_the_measured_sweep():
     from conv2d_batchnorm_silu_gb300 import capi, tune
     expected = {
         "stem640": "thin-input", "down320": "wres", "c2f160_1x1": "rows", "bneck160": "wres",
-        "down160": "swap", "c2f80_1x1": "rows", "bneck80": "swap", "down80": "rows",
+        "down160": "swap", "c2f80_1x1": "rows", "bneck80": "swap", "down80": "swap",
         "c2f40_1x1": "rows", "bneck40": "swap", "down40": "swap", "c2f20_1x1": "rows",
         "bneck20": "swap", "sppf20_1x1": "rows", "head80_3x3": "swap", "tiny": "n32",
         "stem": "thin-input", "down": "rows", "pointwise": "rows", "deep": "n256-sk-pair",
