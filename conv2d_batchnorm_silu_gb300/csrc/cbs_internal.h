@@ -80,8 +80,9 @@ __host__ __device__ constexpr int tc_threads(int block_n, bool pair)
 // its units with eight).
 constexpr int kCmEpiWarps = 12;
 constexpr int kCmThreads = 128 + 32 * kCmEpiWarps;
-// Stream-K slot words: a ready flag per epilogue warp (at most 12).
-constexpr int kTcFlagsPerSlot = 16;
+// Stream-K slot words: a ready flag per (TMEM lane quarter, 32-column chunk) of a tile of up
+// to 256 columns.
+constexpr int kTcFlagsPerSlot = 32;
 
 // Epilogue geometry of the tensor-core kernel for an N tile of `block_n`
 // channels: `split` warps share each 32-row TMEM lane quarter (each takes

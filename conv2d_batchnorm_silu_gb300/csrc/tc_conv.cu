@@ -236,7 +236,8 @@ struct TcCfg {
     static_assert(STAGES >= 2, "shared memory too small for two stages");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
     static_assert(BN % EC == 0 && NCH >= WPQ, "every epilogue warp owns at least one whole chunk");
-    static_assert(EPI_WARPS <= kTcFlagsPerSlot && THREADS == 128 + 32 * EPI_WARPS, "epilogue warps");
+    static_assert(4 * NCH <= kTcFlagsPerSlot && THREADS == 128 + 32 * EPI_WARPS, "epilogue warps");
+    static_assert((2 * STAGES + 6 + 2 * EPI_WARPS) * 8 + 8 <= BAR_BYTES, "barrier area");
     static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 ||
                       TMEM_COLS == 512,
                   "TMEM allocation must be a power of two >= 32");
@@ -325,6 +326,11 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
     constexpr int CG = PAIR ? 2 : 1;  // tcgen05 CTA group
     using C = TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>;
     constexpr int STAGES = C::STAGES;
+    // Pair tiles: the four warps that load and issue (0-3) have nothing left to do once a
+    // worker's last unit is in TMEM, and join its epilogue as a fourth warp per TMEM lane
+    // quarter (the last tile's epilogue has no K loop under it).  Not with a residual, whose
+    // loads use a barrier per staging buffer of the epilogue warps.
+    constexpr bool HELP = PAIR && !RES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -337,7 +343,8 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
-    uint64_t *rbar = drain + 1;  // residual epilogue: a load barrier per staging buffer of each epilogue warp
+    uint64_t *lastfull = drain + 1;  // pair tiles: the worker's last MMA is done (helpers wait on it)
+    uint64_t *rbar = lastfull + 1;  // residual epilogue: a load barrier per staging buffer of each epilogue warp
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rbar + 2 * C::EPI_WARPS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -358,6 +365,7 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
             dev::mbar_init(dev::smem_u32(&tempty[i]), PAIR ? 2 * C::EPI_WARPS : C::EPI_WARPS);
         }
         dev::mbar_init(dev::smem_u32(drain), 1);
+        dev::mbar_init(dev::smem_u32(lastfull), 1);
         if constexpr (RES)
             for (int i = 0; i < 2 * C::EPI_WARPS; ++i) dev::mbar_init(dev::smem_u32(&rbar[i]), 1);
         *abort_flag = 0;
@@ -571,23 +579,29 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
                 else
                     dev::tc_commit<CG>(dev::smem_u32(&tfull[buf]));
             }
+            // The helpers' one barrier: it completes once, when every MMA above has.
+            if constexpr (HELP) dev::tc_commit_multicast<CG>(dev::smem_u32(lastfull), (uint16_t)0x3);
             // All MMAs issued by this thread must finish before TMEM is freed.
             dev::tc_commit<CG>(dev::smem_u32(drain));
             if (!dev::mbar_wait_bounded(dev::smem_u32(drain), 0, nullptr, kWaitTimeoutNs))
                 record_error(kErrTimeoutDrain, abort_flag);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp - 4 < C::EPI_WARPS) {
+    }
+    if ((warp >= 4 && warp - 4 < C::EPI_WARPS) || (HELP && warp < 4)) {
         // ------------------------------------------------------------ epilogue
         constexpr int EC = C::EC;
         constexpr int ROW_Y = EC * 2;
         const int ew = warp & 3;          // this warp may access TMEM lanes [32*ew, 32*ew+32)
-        const int ep = warp - 4;          // epilogue warp index
-        // This warp's chunks of a pixel-major tile: `own` chunks from column col_base.
-        const int c_lo = (ep >> 2) * C::NCH / C::WPQ;
-        const int own = ((ep >> 2) + 1) * C::NCH / C::WPQ - c_lo;
-        const int col_base = c_lo * EC;
-        uint8_t *my_stg = sm_stg + ep * 2 * C::STG_BYTES;
+        const bool helper = warp < 4;     // a loading or issuing warp: the last unit only
+        const int ep = helper ? C::EPI_WARPS + warp : warp - 4;  // epilogue warp index
+        // This warp's chunks of a pixel-major tile: `own` chunks from column col_base (set per
+        // unit where the last unit is split four ways).
+        int c_lo = (ep >> 2) * C::NCH / C::WPQ;
+        int own = ((ep >> 2) + 1) * C::NCH / C::WPQ - c_lo;
+        int col_base = c_lo * EC;
+        // A helper stages its stores in the operand ring, idle once the last unit's MMAs are done.
+        uint8_t *my_stg = helper ? sm_a + warp * 2 * C::STG_BYTES : sm_stg + ep * 2 * C::STG_BYTES;
         int sbuf = 0;
         int lt = 0;
         // Residual epilogue: the residual's tile for a chunk is loaded by TMA into the
@@ -666,6 +680,17 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
         for (; wi.next(a, u); ++lt) {
             const int buf = lt & 1;
             const uint32_t tparity = (uint32_t)(lt >> 1) & 1u;
+            if constexpr (HELP) {
+                // The worker's last unit: four warps per lane quarter, two chunks each.
+                WorkIter nx = wi;
+                WorkUnit q;
+                const bool last = !nx.next(a, q);
+                if (helper && !last) continue;
+                const int parts = last ? C::WPQ + 1 : C::WPQ;
+                c_lo = (ep >> 2) * C::NCH / parts;
+                own = ((ep >> 2) + 1) * C::NCH / parts - c_lo;
+                col_base = c_lo * EC;
+            }
             // Stream-K, pixel-major tiles: the two pieces of a split tile (the head of one
             // worker's range and the tail of the next one's) meet in the slot of that worker
             // boundary; a pair keeps one partial tile per M half.  Each worker runs its tail
@@ -697,17 +722,21 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
                     if (c < a.c_out && c < c0 + own * EC) prefetch_l1(lane < NP ? a.scale + c : a.bias + c);
                 }
             }
-            // Stream-K combine: the partner's flag is nearly always raised before this unit's
-            // accumulator is ready.  Reading it now, while the warp waits anyway, keeps the
-            // load's L2 round trip (~1 us at the end of the kernel) out of the epilogue.
-            int flag_seen = 0;
-            if (combine && lane == 0) flag_seen = ld_acquire_gpu(a.flags + slot * kTcFlagsPerSlot + ep) != 0;
+            // Stream-K flags: one per (lane quarter, 32-column chunk) of the tile, so that the two
+            // pieces of a tile may split its columns among their warps differently.  A combining
+            // warp reads its chunks' flags now, while it waits for the accumulator anyway: they
+            // are nearly always up by then, and the loads' L2 round trip (~1 us at the end of the
+            // kernel) stays out of the epilogue.
+            int *const fl = split ? a.flags + slot * kTcFlagsPerSlot + ew * C::NCH + c_lo : nullptr;
+            uint32_t seen = 0;  // combine: this warp's chunks whose flag is already up
+            if (combine) seen = __ballot_sync(0xffffffffu, lane < own && ld_acquire_gpu(fl + lane) != 0);
+            // A helper comes to its wait after an unknown number of the buffer's earlier phases
+            // (a parity wait only tells the last two apart), so it waits on a barrier of its own
+            // that completes once, after the worker's last MMA.
+            const uint32_t fbar = helper ? dev::smem_u32(lastfull) : dev::smem_u32(&tfull[buf]);
+            const uint32_t fpar = helper ? 0u : tparity;
             int ok = 1;
-            if (lane == 0)
-                ok = dev::mbar_wait_bounded(dev::smem_u32(&tfull[buf]), tparity, abort_flag,
-                                            a.wait_ns)
-                         ? 1
-                         : 0;
+            if (lane == 0) ok = dev::mbar_wait_bounded(fbar, fpar, abort_flag, a.wait_ns) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0 && !*abort_flag) record_error(kErrTimeoutEpilogue, abort_flag);
@@ -809,20 +838,7 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
             const int m_tile = PAIR ? 2 * m_unit + rank : m_unit;
             const int n0 = (u.tile - m_unit * a.n_tiles) * BN;
             const int row0 = m_tile * C::BM + ew * 32;  // first output pixel of this warp
-            if (combine) {
-                int got = 1;
-                if (lane == 0 && !flag_seen)
-                    got = wait_flag_bounded(a.flags + slot * kTcFlagsPerSlot + ep, abort_flag, a.wait_ns) ? 1 : 0;
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) {
-                    if (lane == 0 && !*abort_flag) record_error(kErrTimeoutEpilogue, abort_flag);
-                    break;
-                }
-                // Lane 0's acquire load saw the flag (here or before the accumulator wait); the
-                // warp barrier orders it before every lane's reads of the partial sums.  (A sequentially consistent GPU-scope fence
-                // here cost ~2 us per combined tile, on the kernel's critical path.)
-                __syncwarp();
-            }
+            bool timed_out = false;
             const uint32_t t_lane =
                 tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(buf * BN + col_base);
 #pragma unroll 1
@@ -831,7 +847,7 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
                 // is stored (nor published), and it must not touch a staging buffer either, since
                 // the wait before each staging write counts one store per staged chunk.
                 if (row0 >= a.m || n0 + col_base + j * EC >= a.c_out) {
-                    if (j == own - 1) {
+                    if (j == own - 1 && !helper) {
                         dev::tc_fence_before_sync();
                         __syncwarp();
                         if (lane == 0) {
@@ -852,8 +868,9 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
                 dev::tmem_ld_wait();
 #pragma unroll
                 for (int q = 0; q < EC / 16; ++q) dev::reg_fence16(v + q * 16);
-                if (j == own - 1) {
-                    // The accumulator is in registers: hand the TMEM buffer back to the MMA warp.
+                if (j == own - 1 && !helper) {
+                    // The accumulator is in registers: hand the TMEM buffer back to the MMA warp
+                    // (the helpers read the last unit, which the MMA warp does not wait for).
                     dev::tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
@@ -870,9 +887,27 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
                         __stcg(part + (size_t)((col_base + j * EC) / 4 + q) * C::BM + row,
                                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+                    // The warp barrier orders every lane's stores of the chunk before lane 0's
+                    // release store of its flag, which makes them visible with it GPU-wide.  (A
+                    // sequentially consistent GPU-scope fence on either side of this handoff
+                    // cost ~2 us per combined tile, on the kernel's critical path.)
+                    __syncwarp();
+                    if (lane == 0) st_release_gpu(fl + j, 1);
                     continue;
                 }
                 if (combine) {
+                    if (!((seen >> j) & 1u)) {
+                        int got = 1;
+                        if (lane == 0) got = wait_flag_bounded(fl + j, abort_flag, a.wait_ns) ? 1 : 0;
+                        if (!__shfl_sync(0xffffffffu, got, 0)) {
+                            if (lane == 0 && !*abort_flag) record_error(kErrTimeoutEpilogue, abort_flag);
+                            timed_out = true;
+                            break;
+                        }
+                    }
+                    // The flag was seen by an acquire load of one lane; the warp barrier orders
+                    // that before every lane's loads of the partial sums.
+                    __syncwarp();
 #pragma unroll
                     for (int q = 0; q < EC / 4; ++q) {
                         const float4 p4 = __ldcg(part + (size_t)((col_base + j * EC) / 4 + q) * C::BM + row);
@@ -881,6 +916,9 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
                         v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + p4.z);
                         v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + p4.w);
                     }
+                    // The chunk's partial sums are read: its flag goes back down for the next
+                    // launch (nothing else in this one waits for it).
+                    if (lane == 0) st_release_gpu(fl + j, 0);
                 }
                 const int ch0 = n0 + col_base + j * EC;
                 uint32_t packed[EC / 2];
@@ -991,15 +1029,7 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
                 }
                 sbuf ^= 1;
             }
-            if (publish) {
-                // The warp barrier orders every lane's partial-sum stores before lane 0's
-                // release store of the flag, which makes them visible with it GPU-wide.
-                __syncwarp();
-                if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 1);
-            } else if (combine) {
-                __syncwarp();  // all lanes have read the partial: the slot is free again
-                if (lane == 0) st_release_gpu(a.flags + slot * kTcFlagsPerSlot + ep, 0);
-            }
+            if (timed_out) break;
         }
         if constexpr (RES) {
             // Only after a wait ran out can a load still be in flight: wait for it once more
