@@ -61,7 +61,7 @@ struct TcArgs {
     int stream_k;    // 1: each CTA takes an equal share of all K steps (see WorkIter)
     unsigned long long wait_ns;  // bound on every pipeline wait (draining copies in flight keeps 2 s)
     float *partial;  // stream-K: [grid-1][128*BN] fp32 partial tiles (slot c: boundary of CTAs c, c+1)
-    int *flags;      // stream-K: per slot, a ready flag and an arrival ticket per epilogue warp; 0 between launches
+    int *flags;      // stream-K: per slot, a ready flag per (lane quarter, 32-column chunk); 0 between launches
     int balanced;    // swap AB: each CTA takes an equal run of 32-pixel chunks (see WorkIter)
     int chunks_m;    // balanced: 32-pixel chunks per channel tile, ceil(m / 32)
 };

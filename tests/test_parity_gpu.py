@@ -279,10 +279,16 @@ STREAM_K_CASES = [
     (32, 20, 20, 128, 512, 3, 3, 1, 1),   # 200 tiles, 18 K steps
     (39, 20, 20, 256, 384, 3, 3, 1, 1),   # 244 tiles, ragged last M tile, a 128-channel N tail
     (31, 20, 20, 128, 512, 3, 3, 1, 1),   # 97 M tiles: the last CTA pair's odd half is past the end
+    # 2-CTA pairs whose second 256-channel tile is mostly past c_out: chunks with no channel are
+    # neither published nor combined (per-chunk stream-K flags), on units split three ways and,
+    # for each worker's last unit, four ways
+    (33, 20, 20, 128, 264, 3, 3, 1, 1),   # an 8-channel N tail and a ragged M tail
+    (32, 20, 20, 128, 320, 3, 3, 1, 1),   # a 64-channel N tail
 ]
 
 
-@pytest.mark.parametrize("case", STREAM_K_CASES, ids=["200tiles", "244tiles_ragged", "odd_m_tiles"])
+@pytest.mark.parametrize("case", STREAM_K_CASES,
+                         ids=["200tiles", "244tiles_ragged", "odd_m_tiles", "n_tail_8", "n_tail_64"])
 def test_stream_k_split_tiles(capi, case):
     """Shapes whose plan splits the K loop of some tiles between two CTAs (stream-K):
     every output matches the oracle and two runs are bit-identical (the partial sums
