@@ -82,7 +82,7 @@ struct WorkUnit {
 // of a tile (ke < k_iters: the next CTA holds its tail), never a middle piece.
 struct WorkIter {
     // stream-K state: the worker's range is [tail piece][whole tiles][head piece];
-    // it is processed as tail, head, then whole tiles (see next()).
+    // it is processed as head, tail, then whole tiles (see next()).
     int state;
     int t_tail, kb_tail;   // tail piece: K steps [kb_tail, k_iters) of tile t_tail (kb_tail > 0)
     int t_head, ke_head;   // head piece: K steps [0, ke_head) of tile t_head (ke_head < k_iters)
@@ -122,9 +122,12 @@ struct WorkIter {
             t_full_end = ke1 < a.k_iters ? t1 : t1 + 1;
         }
     }
-    // Stream-K order: the tail piece first, then the head piece, then whole
-    // tiles -- the split pieces meet their other halves (computed early by the
-    // neighbouring workers, too) mid-kernel, and the last epilogue is a plain one.
+    // Stream-K order: the head piece first, then the tail piece, then whole tiles.
+    // Every worker starts at K step 0 of a tile, so the first stages of all CTAs
+    // load the same weight tiles (from a cold L2 the start otherwise pulls most of
+    // the weights at once); the split pieces meet their other halves (published
+    // first by the neighbouring workers) mid-kernel, and the last epilogue of a
+    // worker with whole tiles is a plain one.
     __device__ bool next(const TcArgs &a, WorkUnit &u)
     {
         if (a.balanced) {
@@ -146,19 +149,19 @@ struct WorkIter {
         if (a.stream_k) {
             if (state == 0) {
                 state = 1;
-                if (t_tail >= 0) {
-                    u.tile = t_tail;
-                    u.kb = kb_tail;
-                    u.ke = a.k_iters;
+                if (t_head >= 0) {
+                    u.tile = t_head;
+                    u.kb = 0;
+                    u.ke = ke_head;
                     return true;
                 }
             }
             if (state == 1) {
                 state = 2;
-                if (t_head >= 0) {
-                    u.tile = t_head;
-                    u.kb = 0;
-                    u.ke = ke_head;
+                if (t_tail >= 0) {
+                    u.tile = t_tail;
+                    u.kb = kb_tail;
+                    u.ke = a.k_iters;
                     return true;
                 }
             }
@@ -693,13 +696,13 @@ __global__ void __launch_bounds__(TcCfg<BN, BK, PAIR ? BN / 2 : BN, PAIR>::THREA
             }
             // Stream-K, pixel-major tiles: the two pieces of a split tile (the head of one
             // worker's range and the tail of the next one's) meet in the slot of that worker
-            // boundary; a pair keeps one partial tile per M half.  Each worker runs its tail
-            // piece first, so the tail piece publishes its fp32 partial sums and the head
+            // boundary; a pair keeps one partial tile per M half.  Each worker runs its head
+            // piece first, so the head piece publishes its fp32 partial sums and the tail
             // piece, which its worker runs later, adds them and finishes the tile.  A sum of
             // two fp32 values does not depend on their order: the result is deterministic.
             const bool split = !SWAP && a.stream_k && (u.kb > 0 || u.ke < a.k_iters);
-            const bool publish = split && u.kb > 0;
-            const bool combine = split && u.kb == 0;
+            const bool publish = split && u.kb == 0;
+            const bool combine = split && u.kb > 0;
             const int slot = (u.kb > 0 ? vb - 1 : vb) * (PAIR ? 2 : 1) + rank;
             float4 *part = a.stream_k ? reinterpret_cast<float4 *>(a.partial) + (size_t)slot * (32 * BN)
                                       : nullptr;
